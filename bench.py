@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of the bf16 GEMM / grouped GEMM hot path (TFLOP/s, % of dense-bf16 peak).
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * dense GEMM M=N=K=4096, A row-major, B column-major, U(-1,1), fused
+    bias + GELU(tanh), bf16 out (seed 1), and
+  * grouped MoE GEMM, 64 experts, K=4096, N=1536, 65536 tokens split by a
+    Dirichlet(0.5) multinomial (seed 3), bf16 out,
+each one launch of the persistent kernel through the C ABI.  value = FLOPs of
+the step / device time of the step (CUDA events on the launching stream).
+L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer outside
+the timed events.  `e2e` times the same steps through the public API with the
+inputs copied from pinned host memory every step and C read back.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload (independent
+problems, weak scaling, no data-path collective); the time is the max over ranks
+and value is the work of all ranks over that time.  `--impl reference` times
+the CPU oracle (the plain fp64 definition) on bounded samples of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "dense4096_bias_gelu+grouped_moe"
+WORKLOADS = {
+    HEADLINE: ["dense_4096_bias_gelu", "grouped_moe"],
+    "dense_4096_bias_gelu": ["dense_4096_bias_gelu"],
+    "dense_8192_f32": ["dense_8192_f32"],
+    "grouped_moe": ["grouped_moe"],
+    "skinny_bcast": ["skinny_bcast"],
+    "dense_256": ["dense_256"],
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "bf16 GEMM TFLOP/s and % of GB300 dense-BF16 peak (dense + grouped)"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------------------------------
+# distributed plumbing (host side; the data path has no collective)
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(step_ms_per_rank: list[float], flops_per_rank: float) -> dict:
+    """Whole-job numbers from per-rank step times: the job is as slow as its slowest rank."""
+    world = len(step_ms_per_rank)
+    t = max(step_ms_per_rank)
+    return {"ms_per_step": t, "value_tflops": world * flops_per_rank / (t * 1e-3) / 1e12}
+
+
+def gather_max(x: float, world: int) -> list[float]:
+    if world == 1:
+        return [x]
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [float(v.item()) for v in out]
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------
+# peaks, clocks, traffic
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, _, flags in rows for i, f in enumerate(flags) if f.lower() == "active"})
+        pmax = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows), "power_w_max": pmax}
+
+
+def recorded_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    from grouped_gemm_persistent_gb300.build import _digest
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = _digest([])[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) == 4 and parts[0] == "traffic" and parts[1] == kernel_key and parts[2] == digest:
+            return int(parts[3])
+    return None
+
+
+# ------------------------------------------------------------------------------------------
+# workload construction (inputs generated on the CPU from the seeded generators)
+
+class Part:
+    def __init__(self, name):
+        from grouped_gemm_persistent_gb300 import workloads as wl
+        self.name = name
+        self.grouped = name in wl.GROUPED_WORKLOADS
+        self.case = wl.grouped_case(name) if self.grouped else wl.dense_case(name)
+        self.flops = self.case.flops
+        self.bytes = self.case.algorithmic_bytes
+
+    def describe(self):
+        c = self.case
+        if self.grouped:
+            return {"name": self.name, "G": c.G, "K": c.K, "N": c.N, "tokens": int(c.counts.sum()),
+                    "empty_groups": int((c.counts == 0).sum()), "out": c.c_dtype, "epilogue": c.epi,
+                    "inputs": c.recipe}
+        return {"name": self.name, "M": c.M, "N": c.N, "K": c.K, "a": "col" if c.a_col_major else "row",
+                "b": "col" if c.b_col_major else "row", "out": c.c_dtype, "epilogue": c.epi, "inputs": c.recipe}
+
+    # -- device side
+    def to_device(self, torch):
+        c = self.case
+        self.host = {"a": c.a.contiguous().pin_memory(), "b": c.b.contiguous().pin_memory()}
+        if c.bias is not None:
+            self.host["bias"] = c.bias.contiguous().pin_memory()
+        self.dev = {k: v.cuda() for k, v in self.host.items()}
+        dt = torch.float32 if c.c_dtype == "f32" else torch.bfloat16
+        rows = int(c.counts.sum()) if self.grouped else c.M
+        self.dev["out"] = torch.empty((rows, c.N), dtype=dt, device="cuda")
+        self.host["out"] = torch.empty((rows, c.N), dtype=dt).pin_memory()
+        if self.grouped:
+            import grouped_gemm_persistent_gb300 as tg
+            self.table = tg.build_moe_table(self.dev["a"], self.dev["b"], c.counts, self.dev["out"],
+                                            bias=self.dev.get("bias"), epilogue=c.epi)
+        self.h2d_bytes = sum(v.numel() * v.element_size() for k, v in self.host.items() if k != "out")
+        self.d2h_bytes = self.host["out"].numel() * self.host["out"].element_size()
+
+    def launch(self, stream):
+        import grouped_gemm_persistent_gb300 as tg
+        c, d = self.case, self.dev
+        if self.grouped:
+            tg.grouped_gemm_table(self.table, stream)
+        else:
+            a = d["a"].t() if c.a_col_major else d["a"]
+            b = d["b"].t() if c.b_col_major else d["b"]
+            tg.gemm(a, b, d["out"], bias=d.get("bias"), epilogue=c.epi, stream=stream)
+        return 1   # kernel launches made (one class of layouts per grouped call)
+
+    def e2e_step(self, stream):
+        for k, v in self.host.items():
+            if k != "out":
+                self.dev[k].copy_(v, non_blocking=True)
+        n = self.launch(stream)
+        self.host["out"].copy_(self.dev["out"], non_blocking=True)
+        return n
+
+    # -- oracle side (CPU baseline): rows of this part, FLOPs done
+    def oracle_rows(self, n_rows: int, seed: int):
+        import oracle
+        from grouped_gemm_persistent_gb300 import workloads as wl
+        c = self.case
+        rng = np.random.default_rng(seed)
+        if self.grouped:
+            g = int(np.argmax(c.counts))
+            r0, r1 = c.offsets[g], c.offsets[g + 1]
+            rows = np.sort(rng.choice(r1 - r0, size=min(n_rows, r1 - r0), replace=False))
+            oracle.gemm(wl.bf16_bits(c.a[r0:r1]), wl.bf16_bits(c.b[g]), rows=rows)
+            return 2 * len(rows) * c.N * c.K
+        rows = np.sort(rng.choice(c.M, size=min(n_rows, c.M), replace=False))
+        bias = wl.bf16_bits(c.bias) if c.bias is not None else None
+        oracle.gemm(wl.bf16_bits(c.a), wl.bf16_bits(c.b), a_col_major=c.a_col_major, b_col_major=c.b_col_major,
+                    bias=bias, epi=c.epi, rows=rows)
+        return 2 * len(rows) * c.N * c.K
+
+
+def oracle_sample(parts, target_s: float, seed: int = 0):
+    """Time the oracle on growing row samples of every part until about target_s seconds of work."""
+    import oracle
+    flops, secs, rows_done = 0, 0.0, {}
+    n = 8
+    share = target_s / len(parts)
+    for p in parts:
+        spent, r_total = 0.0, 0
+        n = 8
+        while spent < share:
+            t0 = time.perf_counter()
+            f = p.oracle_rows(n, seed + r_total)
+            dt = time.perf_counter() - t0
+            flops += f
+            spent += dt
+            r_total += n
+            if spent < share:
+                n = int(min(max(n * 2, n * (share - spent) / max(dt, 1e-3)), 4096))
+        secs += spent
+        rows_done[p.name] = r_total
+    return {"flops": flops, "seconds": secs, "rows": rows_done, "cores": oracle.num_threads()}
+
+
+# ------------------------------------------------------------------------------------------
+# arms
+
+def run_reference(args, parts_names):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    parts = [Part(n) for n in parts_names]
+    per_step_s = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(parts, per_step_s / 4)
+    times, flops = [], 0
+    for i in range(args.steps):
+        r = oracle_sample(parts, per_step_s, seed=1000 + i)
+        times.append(r["seconds"])
+        flops += r["flops"]
+    total = sum(times)
+    value = flops / total / 1e12
+    sample = (f"each step: oracle (fp64 CPU) on random output rows of every part, about {per_step_s:.1f} s of work; "
+              f"last step rows {r['rows']}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "parts": [p.describe() for p in parts]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, parts_names):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import grouped_gemm_persistent_gb300 as tg
+    from grouped_gemm_persistent_gb300.build import build
+    if rank == 0:
+        build()
+    barrier(world)
+    tg.load()
+
+    t0 = time.perf_counter()
+    parts = [Part(n) for n in parts_names]
+    for p in parts:
+        p.to_device(torch)
+    log(f"[bench] inputs ready in {time.perf_counter() - t0:.1f} s")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    step_flops = sum(p.flops for p in parts)
+
+    for _ in range(args.warmup):
+        for p in parts:
+            p.launch(stream)
+    tg.device_status(stream)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()                     # L2 flush, outside the timed events
+            ev[i][0].record(stream)
+            for j, p in enumerate(parts):
+                launches += p.launch(stream)
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    tg.device_status(stream)
+    part_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(len(parts))]
+    step_ms = sum(statistics.fmean(x) for x in part_ms)
+    agg = aggregate(gather_max(step_ms, world), step_flops)
+
+    # end to end through the public API: pinned host inputs in, C out, every step
+    e2e = None
+    if not args.no_e2e:
+        for p in parts:
+            p.e2e_step(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        launches_e2e = 0
+        for _ in range(args.steps):
+            for p in parts:
+                launches_e2e += p.e2e_step(stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        tg.device_status(stream)
+        e2e_ms = s0.elapsed_time(s1) / args.steps
+        e2e_agg = aggregate(gather_max(e2e_ms, world), step_flops)
+        e2e = {"value": e2e_agg["value_tflops"], "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(p.h2d_bytes for p in parts),
+               "d2h_bytes_per_step": sum(p.d2h_bytes for p in parts),
+               "ms_per_step": e2e_agg["ms_per_step"], "gpu_launches": launches_e2e}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    # dominant kernel: the part with the largest device time
+    dom = max(range(len(parts)), key=lambda j: statistics.fmean(part_ms[j]))
+    dp = parts[dom]
+    dom_ms = statistics.fmean(part_ms[dom])
+    achieved = dp.flops / (dom_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = recorded_traffic(dp.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": f"gemm_kernel ({dp.name})",
+                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "algorithmic_bytes": dp.bytes}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        r = oracle_sample(parts, args.cpu_seconds)
+        cpu = {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+               "sample": f"oracle (fp64 CPU) on random output rows {r['rows']} of the step's parts, "
+                         f"{r['seconds']:.1f} s"}
+
+    parts_out = []
+    for j, p in enumerate(parts):
+        ms = statistics.fmean(part_ms[j])
+        parts_out.append({**p.describe(), "ms": ms, "tflops": p.flops / (ms * 1e-3) / 1e12,
+                          "frac_of_peak": p.flops / (ms * 1e-3) / 1e12 / peak,
+                          "roofline_ms": 1e3 * max(p.flops / (peak * 1e12), p.bytes / (peaks["hbm_gbs"] * 1e9))})
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": agg["value_tflops"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "parts": parts_out, "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
+                   "frac_of_peak": agg["value_tflops"] / (world * peak)},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        log("[bench] warm-up below 3 steps is not a valid measurement; using 3")
+        args.warmup = 3
+    names = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, names)
+    return run_ours(args, names)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,220 @@
+"""ctypes binding of libtg (include/tg.h).  Argument marshalling only.
+
+Every compute step runs in the CUDA kernels of libtg.so.  There is no Python,
+PyTorch or CPU fallback: if the library is not built, or the device is not a
+GB300 (sm_103a), these functions raise.  PyTorch supplies device memory and
+streams; tensors are passed as raw device pointers with their strides.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtg.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "tg.h")
+
+TG_OK, TG_ERR_INVALID_ARG, TG_ERR_UNSUPPORTED, TG_ERR_CUDA, TG_ERR_TIMEOUT, TG_ERR_NO_DEVICE = range(6)
+STATUS_NAMES = {0: "TG_OK", 1: "TG_ERR_INVALID_ARG", 2: "TG_ERR_UNSUPPORTED", 3: "TG_ERR_CUDA",
+                4: "TG_ERR_TIMEOUT", 5: "TG_ERR_NO_DEVICE"}
+EPILOGUES = {"none": 0, "bias": 1, "bias_gelu": 2}
+ROW_MAJOR, COL_MAJOR = 0, 1
+BF16, F32 = 0, 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+class TGError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+
+
+class GroupProblem(ctypes.Structure):
+    """Mirror of tg_group_problem (field order and natural alignment as in tg.h)."""
+    _fields_ = [
+        ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("layout_a", ctypes.c_int),
+        ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("layout_b", ctypes.c_int),
+        ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64), ("c_dtype", ctypes.c_int),
+        ("epi", ctypes.c_int),
+        ("bias", ctypes.c_void_p),
+    ]
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/tg.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tg_[a-z_]+)\s*\(", text)))
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libtg.so (built by grouped_gemm_persistent_gb300.build); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libtg.so is not built ({p}); run `python -m grouped_gemm_persistent_gb300.build`")
+        lib = ctypes.CDLL(p)
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        lib.tg_gemm.restype = ci
+        lib.tg_gemm.argtypes = [vp, ci, i64, vp, ci, i64, vp, ci, i64, i64, i64, i64, ci, vp, vp]
+        lib.tg_grouped_gemm.restype = ci
+        lib.tg_grouped_gemm.argtypes = [ctypes.POINTER(GroupProblem), ci, vp]
+        lib.tg_status_string.restype = ctypes.c_char_p
+        lib.tg_status_string.argtypes = [ci]
+        lib.tg_last_error_message.restype = ctypes.c_char_p
+        lib.tg_last_error_message.argtypes = []
+        lib.tg_device_status.restype = ci
+        lib.tg_device_status.argtypes = [vp]
+        lib.tg_set_wait_budget_ms.restype = ci
+        lib.tg_set_wait_budget_ms.argtypes = [ctypes.c_uint32]
+        lib.tg_debug_withhold_stage.restype = ci
+        lib.tg_debug_withhold_stage.argtypes = [i64]
+        lib.tg_version.restype = ctypes.c_uint32
+        lib.tg_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != TG_OK:
+        msg = load().tg_last_error_message().decode(errors="replace")
+        raise TGError(status, msg)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _matrix(t: torch.Tensor, name: str):
+    """(layout, ld) of a 2-D tensor view: row-major if its rows are contiguous, else column-major.
+
+    With a single row (or column) the leading dimension is never used to step;
+    it is then reported as the extent rounded up to 8 elements, which keeps the
+    TMA stride rule satisfied.
+    """
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    r, c = t.shape
+    s0, s1 = t.stride()
+    if s1 == 1 or c == 1:
+        return ROW_MAJOR, (s0 if r > 1 else -(-max(c, 1) // 8) * 8)
+    if s0 == 1 or r == 1:
+        return COL_MAJOR, (s1 if c > 1 else -(-max(r, 1) // 8) * 8)
+    raise ValueError(f"{name}: neither rows nor columns are contiguous (strides {t.stride()})")
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, *, bias: torch.Tensor | None = None,
+         epilogue: str = "none", out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """out[M,N] = epilogue(a[M,K] @ b[K,N]) on the GPU via tg_gemm.
+
+    ``a``/``b`` are bf16 CUDA tensors; each may be a row-major or column-major
+    view (a transposed view of a row-major tensor is column-major).  ``out``
+    (bf16 or fp32, rows contiguous, row stride may exceed N) is allocated if
+    not given.  Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise TypeError("a and b must be torch.bfloat16")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N] bf16 or fp32")
+    la, lda = _matrix(a, "a")
+    lb, ldb = _matrix(b, "b")
+    lc, ldc = _matrix(out, "out")
+    if lc != ROW_MAJOR:
+        raise ValueError("out must be row-major")
+    epi = EPILOGUES[epilogue]
+    if epi and (bias is None or bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("this epilogue needs a contiguous bf16 bias of length N")
+    _check(load().tg_gemm(_ptr(a), la, lda, _ptr(b), lb, ldb, _ptr(out), F32 if out.dtype == torch.float32 else BF16,
+                          ldc, M, N, K, epi, _ptr(bias) if epi else None, _stream_handle(stream)))
+    return out
+
+
+def make_problem(a, b, out, *, bias=None, epilogue="none") -> GroupProblem:
+    """One tg_group_problem from tensors (a may have 0 rows: an empty group)."""
+    M, K = a.shape
+    _, N = b.shape
+    la, lda = _matrix(a, "a") if a.numel() else (ROW_MAJOR, max(K, 1))
+    lb, ldb = _matrix(b, "b")
+    _, ldc = _matrix(out, "out") if out.numel() else (ROW_MAJOR, max(N, 1))
+    epi = EPILOGUES[epilogue]
+    return GroupProblem(M, N, K, _ptr(a) if a.numel() else None, lda, la, _ptr(b), ldb, lb,
+                        _ptr(out) if out.numel() else None, ldc, F32 if out.dtype == torch.float32 else BF16, epi,
+                        _ptr(bias) if epi else None)
+
+
+def grouped_gemm_table(table, stream=None) -> None:
+    """Call tg_grouped_gemm on a sequence of GroupProblem (or a ctypes array of them)."""
+    arr = table if isinstance(table, ctypes.Array) else (GroupProblem * len(table))(*table)
+    _check(load().tg_grouped_gemm(arr, len(arr), _stream_handle(stream)))
+
+
+def build_moe_table(a: torch.Tensor, b: torch.Tensor, counts, out: torch.Tensor, *, bias: torch.Tensor | None = None,
+                    epilogue: str = "none") -> ctypes.Array:
+    """The tg_group_problem table of an MoE expert GEMM (see moe_grouped_gemm), built once for reuse."""
+    counts = [int(c) for c in counts]
+    G = len(counts)
+    if b.dim() != 3 or b.shape[0] != G:
+        raise ValueError("b must be [G, K, N] with G = len(counts)")
+    total = sum(counts)
+    if a.shape[0] != total or out.shape[0] != total:
+        raise ValueError(f"a and out need {total} rows (sum of counts)")
+    table = []
+    r = 0
+    for g, m in enumerate(counts):
+        table.append(make_problem(a[r:r + m], b[g], out[r:r + m], bias=None if bias is None else bias[g],
+                                  epilogue=epilogue))
+        r += m
+    return (GroupProblem * G)(*table)
+
+
+def moe_grouped_gemm(a: torch.Tensor, b: torch.Tensor, counts, out: torch.Tensor | None = None, *,
+                     bias: torch.Tensor | None = None, epilogue: str = "none",
+                     out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """MoE expert GEMM: rows of ``a`` [sum M_g, K] grouped by expert (``counts`` on the host),
+    expert g's rows times ``b[g]`` ([G, K, N], each a row- or column-major view) into ``out`` [sum M_g, N].
+    ``bias`` is [G, N] bf16 when the epilogue uses one."""
+    if out is None:
+        out = torch.empty((a.shape[0], b.shape[2]), dtype=out_dtype, device=a.device)
+    grouped_gemm_table(build_moe_table(a, b, counts, out, bias=bias, epilogue=epilogue), stream)
+    return out
+
+
+def device_status(stream=None) -> None:
+    """Synchronise ``stream`` and raise TGError if a kernel reported a timeout or CUDA failed."""
+    _check(load().tg_device_status(_stream_handle(stream)))
+
+
+def set_wait_budget_ms(ms: int) -> None:
+    _check(load().tg_set_wait_budget_ms(ms))
+
+
+def debug_withhold_stage(k_block: int) -> None:
+    _check(load().tg_debug_withhold_stage(k_block))
+
+
+def version() -> tuple[int, int]:
+    v = load().tg_version()
+    return v >> 16, v & 0xFFFF

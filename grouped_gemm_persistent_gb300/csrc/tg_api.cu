@@ -1,0 +1,468 @@
+// tg_api.cu - host side of libtg: the C ABI declared in include/tg.h.
+//
+// Responsibilities: argument checks (before anything is enqueued), TMA tensor
+// map encoding (cuTensorMapEncodeTiled, reached through the runtime's driver
+// entry-point query so the library does not link libcuda), choice of kernel
+// variant and persistent grid size, the grouped problem table (prefix sums of
+// tile counts, copied into a stream-ordered workspace), and the per-device
+// error record written by the kernels' bounded waits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "tg.h"
+#include "tg_launch.cuh"
+
+// Per-device record of the first in-kernel wait that ran out (zero at module load).
+__device__ tg::ErrorRecord g_tg_error;
+
+namespace {
+
+using tg::Config;
+using tg::Params;
+using tg::Problem;
+
+constexpr uint32_t kDefaultBudgetMs = 1000;
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+thread_local std::string t_message;
+thread_local int64_t t_withhold = -1;
+
+std::atomic<uint32_t> g_budget_ms{0};
+
+tg_status fail(tg_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_message = buf;
+    return s;
+}
+
+tg_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? TG_ERR_NO_DEVICE : TG_ERR_CUDA,
+                "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+uint32_t budget_ms() {
+    uint32_t b = g_budget_ms.load();
+    if (b == 0) {
+        const char* env = std::getenv("TG_WAIT_BUDGET_MS");
+        long v = env ? std::strtol(env, nullptr, 10) : 0;
+        b = (v > 0 && v < 3600000) ? static_cast<uint32_t>(v) : kDefaultBudgetMs;
+    }
+    return b;
+}
+
+// ----------------------------------------------------------------------------------------
+// per-device state
+
+struct DeviceState {
+    bool ready = false;
+    int cc_major = 0, cc_minor = 0, sms = 0;
+    tg::ErrorRecord* err = nullptr;
+    cudaMemPool_t pool = nullptr;
+    int units[64] = {};   // resident work units per kernel variant (0 = not yet queried)
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+tg_status device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (d.cc_major != 10 || d.cc_minor != 3)
+            return fail(TG_ERR_UNSUPPORTED, "device %d is sm_%d%d; libtg is built for sm_103a (GB300) only", dev,
+                        d.cc_major, d.cc_minor);
+        void* sym = nullptr;
+        if ((e = cudaGetSymbolAddress(&sym, g_tg_error)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+        d.err = static_cast<tg::ErrorRecord*>(sym);
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = UINT64_MAX;  // keep freed workspace cached in the pool
+        if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemPoolSetAttribute");
+        d.ready = true;
+    }
+    *out = &d;
+    return TG_OK;
+}
+
+// ----------------------------------------------------------------------------------------
+// tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+tg_status encoder() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    static cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSuccess;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+    if (!g_encode) return fail(TG_ERR_CUDA, "driver does not provide cuTensorMapEncodeTiled (query result %d)", int(q));
+    return TG_OK;
+}
+
+tg_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+                   uint64_t ld_bytes, uint32_t box_inner, uint32_t box_outer, const char* what, int g) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_UNSUPPORTED, "problem %d: cuTensorMapEncodeTiled(%s) failed with CUresult %d", g, what,
+                    int(r));
+    return TG_OK;
+}
+
+// ----------------------------------------------------------------------------------------
+// argument checks
+
+struct Prob {
+    const void* A; tg_layout la; int64_t lda;
+    const void* B; tg_layout lb; int64_t ldb;
+    void* C; tg_dtype cd; int64_t ldc;
+    int64_t M, N, K;
+    tg_epilogue epi;
+    const void* bias;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+tg_status check(const Prob& q, int g) {
+    if (q.la != TG_ROW_MAJOR && q.la != TG_COL_MAJOR) return fail(TG_ERR_INVALID_ARG, "problem %d: bad layout_a %d", g, int(q.la));
+    if (q.lb != TG_ROW_MAJOR && q.lb != TG_COL_MAJOR) return fail(TG_ERR_INVALID_ARG, "problem %d: bad layout_b %d", g, int(q.lb));
+    if (q.cd != TG_BF16 && q.cd != TG_F32) return fail(TG_ERR_INVALID_ARG, "problem %d: bad c_dtype %d", g, int(q.cd));
+    if (q.epi != TG_EPI_NONE && q.epi != TG_EPI_BIAS && q.epi != TG_EPI_BIAS_GELU)
+        return fail(TG_ERR_INVALID_ARG, "problem %d: bad epilogue %d", g, int(q.epi));
+    if (q.M < 0 || q.N < 0 || q.K < 0)
+        return fail(TG_ERR_INVALID_ARG, "problem %d: negative size M=%lld N=%lld K=%lld", g, (long long)q.M,
+                    (long long)q.N, (long long)q.K);
+    if (q.M > kMaxDim || q.N > kMaxDim || q.K > kMaxDim)
+        return fail(TG_ERR_UNSUPPORTED, "problem %d: sizes must be below 2^31", g);
+    if (q.M == 0 || q.N == 0) return TG_OK;  // nothing to compute; pointers unused
+
+    if (!q.C) return fail(TG_ERR_INVALID_ARG, "problem %d: C is NULL", g);
+    if (q.ldc < q.N) return fail(TG_ERR_INVALID_ARG, "problem %d: ldc=%lld < N=%lld", g, (long long)q.ldc, (long long)q.N);
+    if (q.epi != TG_EPI_NONE && !q.bias) return fail(TG_ERR_INVALID_ARG, "problem %d: epilogue needs a bias", g);
+    if (q.K > 0) {
+        if (!q.A) return fail(TG_ERR_INVALID_ARG, "problem %d: A is NULL", g);
+        if (!q.B) return fail(TG_ERR_INVALID_ARG, "problem %d: B is NULL", g);
+        const int64_t min_lda = q.la == TG_ROW_MAJOR ? q.K : q.M;
+        const int64_t min_ldb = q.lb == TG_ROW_MAJOR ? q.N : q.K;
+        if (q.lda < min_lda)
+            return fail(TG_ERR_INVALID_ARG, "problem %d: lda=%lld < %lld", g, (long long)q.lda, (long long)min_lda);
+        if (q.ldb < min_ldb)
+            return fail(TG_ERR_INVALID_ARG, "problem %d: ldb=%lld < %lld", g, (long long)q.ldb, (long long)min_ldb);
+        if (q.lda > kMaxDim || q.ldb > kMaxDim) return fail(TG_ERR_UNSUPPORTED, "problem %d: ld must be below 2^31", g);
+        if (!aligned16(q.A) || !aligned16(q.B))
+            return fail(TG_ERR_UNSUPPORTED, "problem %d: A and B must be 16-byte aligned (TMA)", g);
+        if ((q.lda * 2) % 16 || (q.ldb * 2) % 16)
+            return fail(TG_ERR_UNSUPPORTED, "problem %d: lda and ldb must be multiples of 8 bf16 elements (TMA)", g);
+    }
+    const int64_t esize = q.cd == TG_F32 ? 4 : 2;
+    if (q.ldc > kMaxDim) return fail(TG_ERR_UNSUPPORTED, "problem %d: ldc must be below 2^31", g);
+    if (!aligned16(q.C)) return fail(TG_ERR_UNSUPPORTED, "problem %d: C must be 16-byte aligned (TMA)", g);
+    if ((q.ldc * esize) % 16) return fail(TG_ERR_UNSUPPORTED, "problem %d: ldc * element size must be a multiple of 16 bytes (TMA)", g);
+    if (q.bias && (reinterpret_cast<uintptr_t>(q.bias) & 1u)) return fail(TG_ERR_INVALID_ARG, "problem %d: bias is not 2-byte aligned", g);
+    return TG_OK;
+}
+
+// ----------------------------------------------------------------------------------------
+// kernel variants
+
+using LaunchFn = cudaError_t (*)(const Params&, int, cudaStream_t);
+using UnitsFn = cudaError_t (*)(int*);
+struct Variant {
+    LaunchFn launch;
+    UnitsFn units;
+    int bn, cta_group, tile_m, cw, bn_cta;
+};
+
+template <int BN, int CG, bool AMN, bool BMN, bool F32, bool GR>
+constexpr Variant variant() {
+    using C = Config<BN, CG, AMN, BMN, F32, GR>;
+    return Variant{&tg::launch<C>, &tg::resident_units<C>, C::BN, C::CTA_GROUP, C::TILE_M, C::CW, C::BN_CTA};
+}
+
+#define TG_VARIANT_ENTRY(BN, CG, AMN, BMN, F32, GR) variant<BN, CG, AMN, BMN, F32, GR>(),
+
+const Variant kVariants[] = {
+    TG_FOR_EACH_TILE(TG_VARIANT_ENTRY, false, false)
+    TG_FOR_EACH_TILE(TG_VARIANT_ENTRY, true, false)
+    TG_FOR_EACH_TILE(TG_VARIANT_ENTRY, false, true)
+    TG_FOR_EACH_TILE(TG_VARIANT_ENTRY, true, true)
+};
+constexpr int kTilesPerGroup = 8;
+
+int variant_index(bool grouped, bool f32, int bn, bool amn, bool bmn) {
+    const int tile = (bn == 256 ? 4 : 0) + (amn ? 2 : 0) + (bmn ? 1 : 0);
+    return ((grouped ? 2 : 0) + (f32 ? 1 : 0)) * kTilesPerGroup + tile;
+}
+
+tg_status resident(DeviceState* d, int vi, int* units) {
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (d->units[vi] > 0) { *units = d->units[vi]; return TG_OK; }
+    }
+    int u = 0;
+    cudaError_t e = kVariants[vi].units(&u);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (u <= 0) return fail(TG_ERR_UNSUPPORTED, "kernel variant %d cannot be resident on this device", vi);
+    std::lock_guard<std::mutex> lock(g_mu);
+    d->units[vi] = u;
+    *units = u;
+    return TG_OK;
+}
+
+int pick_bn(int64_t max_n) { return max_n > 128 ? 256 : 128; }
+
+// Raster band (N-tiles swept before stepping along M): a square-ish footprint
+// for the tiles that run concurrently, so A rows and B columns are shared in L2.
+int pick_band(int64_t tiles_n, int units) {
+    int band = 1;
+    while (band * band * 2 <= units && band < 16) band *= 2;
+    if (band > tiles_n) band = static_cast<int>(tiles_n);
+    return band < 1 ? 1 : band;
+}
+
+tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
+    std::memset(out, 0, sizeof(Problem));
+    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    tg_status s;
+    if (q.K > 0) {
+        if (q.la == TG_ROW_MAJOR)
+            s = make_map(&out->tma_a, bf16, q.A, q.K, q.M, q.lda * 2, 64, tg::BM, "A", g);
+        else
+            s = make_map(&out->tma_a, bf16, q.A, q.M, q.K, q.lda * 2, 64, 64, "A", g);
+        if (s != TG_OK) return s;
+        if (q.lb == TG_ROW_MAJOR)
+            s = make_map(&out->tma_b, bf16, q.B, q.N, q.K, q.ldb * 2, 64, 64, "B", g);
+        else
+            s = make_map(&out->tma_b, bf16, q.B, q.K, q.N, q.ldb * 2, 64, v.bn_cta, "B", g);
+        if (s != TG_OK) return s;
+    }
+    const bool f32 = q.cd == TG_F32;
+    s = make_map(&out->tma_c, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : bf16, q.C, q.N, q.M, q.ldc * (f32 ? 4 : 2),
+                 v.cw, 32, "C", g);
+    if (s != TG_OK) return s;
+    out->bias = static_cast<const __nv_bfloat16*>(q.epi != TG_EPI_NONE ? q.bias : nullptr);
+    out->M = static_cast<int32_t>(q.M);
+    out->N = static_cast<int32_t>(q.N);
+    out->K = static_cast<int32_t>(q.K);
+    out->epi = static_cast<int32_t>(q.epi);
+    out->tiles_m = static_cast<int32_t>((q.M + v.tile_m - 1) / v.tile_m);
+    out->tiles_n = static_cast<int32_t>((q.N + v.bn - 1) / v.bn);
+    out->k_blocks = static_cast<int32_t>((q.K + tg::BK - 1) / tg::BK);
+    return TG_OK;
+}
+
+void base_params(Params* p, DeviceState* d) {
+    p->err = d->err;
+    p->wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
+    p->withhold_kb = t_withhold;
+    t_withhold = -1;
+}
+
+tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t stream) {
+    int64_t want = p.total_tiles < units ? p.total_tiles : units;
+    const int grid = static_cast<int>(want) * v.cta_group;
+    cudaError_t e = v.launch(p, grid, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return TG_OK;
+}
+
+}  // namespace
+
+// ========================================================================================
+// C ABI
+
+extern "C" {
+
+tg_status tg_gemm(const void* A, tg_layout layout_a, int64_t lda, const void* B, tg_layout layout_b, int64_t ldb,
+                  void* C, tg_dtype c_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K, tg_epilogue epi,
+                  const void* bias, tg_stream_t stream) {
+    const Prob q{A, layout_a, lda, B, layout_b, ldb, C, c_dtype, ldc, M, N, K, epi, bias};
+    tg_status s = check(q, 0);
+    if (s != TG_OK) return s;
+    if (M == 0 || N == 0) return TG_OK;
+    DeviceState* d = nullptr;
+    if ((s = device_state(&d)) != TG_OK) return s;
+    if ((s = encoder()) != TG_OK) return s;
+
+    const int bn = pick_bn(N);
+    const int vi = variant_index(false, c_dtype == TG_F32, bn, layout_a == TG_COL_MAJOR, layout_b == TG_ROW_MAJOR);
+    const Variant& v = kVariants[vi];
+    int units = 0;
+    if ((s = resident(d, vi, &units)) != TG_OK) return s;
+
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    if ((s = fill_problem(q, v, 0, &p.dense)) != TG_OK) return s;
+    p.dense.tile_begin = 0;
+    p.problems = nullptr;
+    p.num_problems = 1;
+    p.total_tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
+    p.band = pick_band(p.dense.tiles_n, units);
+    base_params(&p, d);
+    return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stream) {
+    if (G < 0 || G > 65536) return fail(TG_ERR_INVALID_ARG, "G=%d out of range [0, 65536]", G);
+    if (G == 0) return TG_OK;
+    if (!table) return fail(TG_ERR_INVALID_ARG, "problem table is NULL");
+    std::vector<Prob> qs(G);
+    bool any = false;
+    for (int g = 0; g < G; ++g) {
+        const tg_group_problem& t = table[g];
+        qs[g] = Prob{t.A, t.layout_a, t.lda, t.B, t.layout_b, t.ldb, t.C, t.c_dtype, t.ldc, t.M, t.N, t.K, t.epi, t.bias};
+        tg_status s = check(qs[g], g);
+        if (s != TG_OK) return s;
+        any = any || (t.M > 0 && t.N > 0);
+    }
+    if (!any) return TG_OK;
+    DeviceState* d = nullptr;
+    tg_status s;
+    if ((s = device_state(&d)) != TG_OK) return s;
+    if ((s = encoder()) != TG_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    // One launch per (layout_a, layout_b, c_dtype) class, classes in order of first appearance.
+    std::vector<std::tuple<int, int, int>> order;
+    std::map<std::tuple<int, int, int>, std::vector<int>> classes;
+    for (int g = 0; g < G; ++g) {
+        if (qs[g].M == 0 || qs[g].N == 0) continue;
+        auto key = std::make_tuple(int(qs[g].la), int(qs[g].lb), int(qs[g].cd));
+        auto it = classes.find(key);
+        if (it == classes.end()) { order.push_back(key); classes[key] = {g}; }
+        else it->second.push_back(g);
+    }
+    const int64_t withhold = t_withhold;
+    for (const auto& key : order) {
+        const std::vector<int>& members = classes[key];
+        int64_t max_n = 0;
+        for (int g : members) max_n = qs[g].N > max_n ? qs[g].N : max_n;
+        const int vi = variant_index(true, std::get<2>(key) == TG_F32, pick_bn(max_n), std::get<0>(key) == TG_COL_MAJOR,
+                                     std::get<1>(key) == TG_ROW_MAJOR);
+        const Variant& v = kVariants[vi];
+        int units = 0;
+        if ((s = resident(d, vi, &units)) != TG_OK) return s;
+
+        std::vector<Problem> host(members.size());
+        int64_t tiles = 0, max_tiles_n = 1;
+        for (size_t i = 0; i < members.size(); ++i) {
+            if ((s = fill_problem(qs[members[i]], v, members[i], &host[i])) != TG_OK) return s;
+            host[i].tile_begin = tiles;
+            tiles += static_cast<int64_t>(host[i].tiles_m) * host[i].tiles_n;
+            if (host[i].tiles_n > max_tiles_n) max_tiles_n = host[i].tiles_n;
+        }
+        const size_t bytes = host.size() * sizeof(Problem);
+        void* ws = nullptr;
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, d->pool, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(problem table)");
+        e = cudaMemcpyAsync(ws, host.data(), bytes, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) {
+            cudaFreeAsync(ws, st);
+            return cuda_fail(e, "cudaMemcpyAsync(problem table)");
+        }
+        Params p;
+        std::memset(&p, 0, sizeof p);
+        p.problems = static_cast<const Problem*>(ws);
+        p.num_problems = static_cast<int32_t>(host.size());
+        p.total_tiles = tiles;
+        p.band = pick_band(max_tiles_n, units);
+        t_withhold = withhold;
+        base_params(&p, d);
+        s = enqueue(p, v, units, st);
+        e = cudaFreeAsync(ws, st);
+        if (s != TG_OK) return s;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(problem table)");
+    }
+    t_withhold = -1;
+    return TG_OK;
+}
+
+const char* tg_status_string(tg_status status) {
+    switch (status) {
+        case TG_OK: return "success";
+        case TG_ERR_INVALID_ARG: return "invalid argument";
+        case TG_ERR_UNSUPPORTED: return "unsupported (alignment, size limit or device)";
+        case TG_ERR_CUDA: return "CUDA error";
+        case TG_ERR_TIMEOUT: return "in-kernel wait timed out";
+        case TG_ERR_NO_DEVICE: return "no CUDA device";
+    }
+    return "unknown status";
+}
+
+const char* tg_last_error_message(void) { return t_message.c_str(); }
+
+tg_status tg_device_status(tg_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    DeviceState* d = nullptr;
+    tg_status s = device_state(&d);
+    if (s != TG_OK) return s;
+    tg::ErrorRecord rec;
+    e = cudaMemcpy(&rec, d->err, sizeof rec, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error record");
+    if (rec.code == tg::ERR_NONE) return TG_OK;
+    e = cudaMemset(d->err, 0, sizeof rec);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error record");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error record");
+    static const char* roles[] = {"?", "TMA producer", "MMA issuer", "epilogue", "MMA drain"};
+    return fail(TG_ERR_TIMEOUT, "in-kernel wait ran out: role=%s block=%u stage=%u tile=%lld waited=%.1f ms",
+                rec.role < 5 ? roles[rec.role] : "?", rec.block, rec.stage, (long long)rec.tile,
+                rec.waited_ns / 1e6);
+}
+
+tg_status tg_set_wait_budget_ms(uint32_t ms) {
+    if (ms > 3600000u) return fail(TG_ERR_INVALID_ARG, "wait budget %u ms above one hour", ms);
+    g_budget_ms.store(ms);
+    return TG_OK;
+}
+
+tg_status tg_debug_withhold_stage(int64_t k_block) {
+    if (k_block < -1) return fail(TG_ERR_INVALID_ARG, "k_block must be >= -1");
+    t_withhold = k_block;
+    return TG_OK;
+}
+
+uint32_t tg_version(void) { return (0u << 16) | 1u; }
+
+}  // extern "C"

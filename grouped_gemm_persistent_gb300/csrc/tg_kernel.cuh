@@ -1,0 +1,585 @@
+// tg_kernel.cuh - the persistent, warp-specialised bf16 GEMM / grouped GEMM kernel.
+//
+// Structure (the producer / MMA / epilogue split and the mbarrier-guarded
+// shared-memory ring of the TLX-on-Blackwell matmul listing in "How We Built
+// TLX", section "Introducing TLX"; here re-designed for sm_103a, made
+// persistent, with a double-buffered TMEM accumulator so the epilogue of one
+// tile overlaps the main loop of the next):
+//
+//   warp 0      TMA producer: one thread streams A and B k-blocks into a
+//               STAGES-deep ring; full[s] completes when the bytes land.
+//   warp 1      MMA issuer: one thread waits full[s], issues BK/16 tcgen05.mma
+//               into TMEM accumulator buffer b, commits empty[s] (slot free)
+//               and, after the last k-block, tfull[b] (tile done).  Warp 1
+//               also allocates and frees tensor memory.
+//   warps 2-5   epilogue: wait tfull[b], tcgen05.ld the fp32 accumulator,
+//               release the buffer (tempty[b]), add bias / apply GELU(tanh),
+//               round, stage through swizzled shared memory and TMA-store C.
+//
+// CTA_GROUP == 2 pairs the two CTAs of a cluster on one 256-row tile: each
+// CTA loads its own 128 rows of A and its own half of the tile's B columns
+// into its own shared memory, the leader CTA's MMA thread issues
+// tcgen05.mma.cta_group::2 over both, and each CTA's TMEM receives its 128
+// rows of the accumulator.  No TMA multicast is used.
+//
+// The tile scheduler is static and persistent: work unit u (a CTA, or a CTA
+// pair) takes tiles u, u + U, u + 2U, ... of the concatenated tile list of
+// all problems; within a problem tiles are rastered in bands of `band`
+// N-tiles so that concurrently running tiles share A rows and B columns in L2.
+//
+// Every mbarrier wait is bounded (wait_budget_ns, measured with %globaltimer).
+// On expiry the waiting thread records the failure in the device error
+// record, raises the CTA's abort flag (and its peer's), and all roles leave
+// their loops: in-flight TMA loads are waited for, issued MMAs are drained
+// with a final commit, tensor memory is freed and the kernel returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "tg_ptx.cuh"
+
+namespace tg {
+
+constexpr int BM = 128;              // accumulator rows per CTA (TMEM lanes)
+constexpr int BK = 64;               // K per pipeline stage: one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;           // K per tcgen05.mma.kind::f16
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;         // warps 2..5 drain TMEM; warp w reads lanes 32*(w%4)..+31
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int C_STAGE_BYTES = 32 * 128;   // per-warp store staging buffer: 32 rows x 128 bytes
+constexpr int SMEM_LIMIT = 232448;        // max dynamic shared memory per CTA on sm_100 family
+
+enum : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1 };
+enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4 };
+enum : int32_t { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_GELU = 2 };
+
+struct ErrorRecord {
+    uint32_t code;        // ERR_*
+    uint32_t role;        // ROLE_*
+    uint32_t block;       // blockIdx.x of the reporting CTA
+    uint32_t stage;       // ring stage or accumulator buffer being waited on
+    int64_t tile;         // global tile index
+    uint64_t waited_ns;
+};
+
+// One GEMM problem as the device sees it.
+struct alignas(128) Problem {
+    CUtensorMap tma_a;
+    CUtensorMap tma_b;
+    CUtensorMap tma_c;
+    const __nv_bfloat16* bias;
+    int64_t tile_begin;   // global index of this problem's first tile
+    int32_t M, N, K;
+    int32_t epi;
+    int32_t tiles_m, tiles_n, k_blocks;
+    int32_t reserved;
+};
+
+struct Params {
+    Problem dense;              // the problem of a dense launch (lives in parameter space)
+    const Problem* problems;    // grouped launch: device array written by the host
+    int32_t num_problems;
+    int32_t band;               // raster band width in N-tiles
+    int64_t total_tiles;
+    ErrorRecord* err;
+    uint64_t wait_budget_ns;
+    int64_t withhold_kb;        // test hook, -1 = off (see tg_debug_withhold_stage)
+};
+
+template <int BN_, int CTA_GROUP_, bool A_MN_, bool B_MN_, bool C_F32_, bool GROUPED_>
+struct Config {
+    static constexpr int BN = BN_;                   // tile columns (whole pair)
+    static constexpr int CTA_GROUP = CTA_GROUP_;
+    static constexpr bool A_MN = A_MN_;              // A stored M-contiguous (column-major)
+    static constexpr bool B_MN = B_MN_;              // B stored N-contiguous (row-major K x N)
+    static constexpr bool C_F32 = C_F32_;
+    static constexpr bool GROUPED = GROUPED_;
+    static constexpr int BN_CTA = BN / CTA_GROUP;    // B columns each CTA loads
+    static constexpr int TILE_M = BM * CTA_GROUP;    // rows per tile (pair)
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN_CTA * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int CW = C_F32 ? 32 : 64;       // output columns per 128-byte staged row
+    static constexpr int TMEM_COLS = 2 * BN;         // two fp32 accumulators of BN columns
+    static constexpr int C_BYTES = NUM_EPI_WARPS * 2 * C_STAGE_BYTES;
+    static constexpr int BIAS_BYTES = NUM_EPI_WARPS * BN * 2;
+    static constexpr int FIXED = C_BYTES + BIAS_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BIAS = OFF_C + C_BYTES;
+    static constexpr int OFF_BAR = OFF_BIAS + BIAS_BYTES;
+    // barriers: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
+    static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+    static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+
+    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TILE_M, BN, A_MN, B_MN);
+
+    static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "cta group");
+    static_assert(STAGES >= 2, "ring too shallow");
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+    static_assert(BN_CTA % 64 == 0, "MN-major B is loaded in 64-column boxes");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
+};
+
+// ----------------------------------------------------------------------------------------
+// scheduling helpers
+
+struct TileCoord {
+    int g;        // problem index
+    int m0;       // first accumulator row of this CTA
+    int n0;       // first column of the tile
+};
+
+template <class Cfg>
+__device__ __forceinline__ const Problem& problem_of(const Params& p, int g) {
+    if constexpr (Cfg::GROUPED) return p.problems[g];
+    else return p.dense;
+}
+
+// Problem containing global tile t; `g` is a hint that only moves forward.
+template <class Cfg>
+__device__ __forceinline__ int find_problem(const Params& p, int64_t t, int g) {
+    if constexpr (Cfg::GROUPED) {
+        while (g + 1 < p.num_problems && p.problems[g + 1].tile_begin <= t) ++g;
+        return g;
+    } else {
+        return 0;
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int g, uint32_t rank) {
+    const Problem& pr = problem_of<Cfg>(p, g);
+    const int64_t local = t - pr.tile_begin;
+    const int band = p.band;
+    const int64_t per_band = static_cast<int64_t>(pr.tiles_m) * band;
+    const int b = static_cast<int>(local / per_band);
+    const int r = static_cast<int>(local - static_cast<int64_t>(b) * per_band);
+    const int n_first = b * band;
+    const int width = min(band, pr.tiles_n - n_first);
+    const int mb = r / width;
+    const int nb = n_first + (r - mb * width);
+    TileCoord c;
+    c.g = g;
+    c.m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
+    c.n0 = nb * Cfg::BN;
+    return c;
+}
+
+// ----------------------------------------------------------------------------------------
+// bounded waits
+
+__device__ __forceinline__ void report_timeout(const Params& p, uint32_t role, int64_t tile, uint32_t stage,
+                                               uint64_t waited) {
+    if (atomicCAS(&p.err->code, ERR_NONE, ERR_TIMEOUT) == ERR_NONE) {
+        p.err->role = role;
+        p.err->block = blockIdx.x;
+        p.err->stage = stage;
+        p.err->tile = tile;
+        p.err->waited_ns = waited;
+        __threadfence();
+    }
+}
+
+// Raise the abort flag of this CTA and, in a pair, of the peer CTA.
+template <int CTA_GROUP>
+__device__ __forceinline__ void raise_abort(uint32_t abort_addr) {
+    asm volatile("st.volatile.shared::cta.u32 [%0], 1;" :: "r"(abort_addr) : "memory");
+    if constexpr (CTA_GROUP == 2) {
+        const uint32_t peer = ptx::mapa(abort_addr, ptx::cluster_ctarank() ^ 1u);
+        asm volatile("st.relaxed.cluster.shared::cluster.u32 [%0], 1;" :: "r"(peer) : "memory");
+    }
+}
+
+__device__ __forceinline__ bool abort_raised(uint32_t abort_addr) {
+    uint32_t v;
+    asm volatile("ld.volatile.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(abort_addr) : "memory");
+    return v != 0;
+}
+
+// Wait for phase `parity` of `bar`.  false: the budget ran out (recorded) or
+// another role aborted; the caller leaves its loop.
+template <int CTA_GROUP>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& p, uint32_t abort_addr,
+                                             uint32_t role, int64_t tile, uint32_t stage) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 0u) {
+            if (abort_raised(abort_addr)) return false;
+            const uint64_t dt = ptx::globaltimer_ns() - t0;
+            if (dt > p.wait_budget_ns) {
+                report_timeout(p, role, tile, stage, dt);
+                raise_abort<CTA_GROUP>(abort_addr);
+                return false;
+            }
+        }
+    }
+}
+
+// Quiet wait used while shutting down after an abort: no new error record.
+__device__ __forceinline__ bool wait_quiet(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > budget_ns) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void sleep_ns(uint64_t ns) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < ns) __nanosleep(1000);
+}
+
+// ----------------------------------------------------------------------------------------
+// epilogue math
+
+__device__ __forceinline__ float gelu_tanh_f32(float z) {
+    // z/2 * (1 + tanh(sqrt(2/pi) * (z + 0.044715 z^3)))
+    const float k0 = 0.7978845608028654f;
+    const float k1 = 0.044715f;
+    const float u = k0 * fmaf(k1 * z, z * z, z);
+    return 0.5f * z * (1.0f + ptx::tanh_approx(u));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ----------------------------------------------------------------------------------------
+// the kernel
+
+template <class Cfg>
+__global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_constant__ Params p) {
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int CG = Cfg::CTA_GROUP;
+    constexpr int BN = Cfg::BN;
+
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms (same offset in every CTA).
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw);
+
+    const uint32_t sA = base + Cfg::OFF_A;
+    const uint32_t sB = base + Cfg::OFF_B;
+    const uint32_t sC = base + Cfg::OFF_C;
+    const uint32_t bar0 = base + Cfg::OFF_BAR;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t tmem_slot = base + Cfg::OFF_TMEM_SLOT;
+    const uint32_t abort_addr = base + Cfg::OFF_ABORT;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = (CG == 2) ? ptx::cluster_ctarank() : 0u;
+    const bool leader = (rank == 0);
+    const int64_t unit = blockIdx.x / CG;
+    const int64_t num_units = gridDim.x / CG;
+
+    // ---- set-up: barriers, tensor memory
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(tfull_bar(b), 1);
+            ptx::mbar_init(tempty_bar(b), NUM_EPI_WARPS * CG);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        asm volatile("st.shared::cta.u32 [%0], 0;" :: "r"(abort_addr) : "memory");
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<CG>(tmem_slot, Cfg::TMEM_COLS);
+        ptx::tmem_relinquish<CG>();
+    }
+    if constexpr (!Cfg::GROUPED) {
+        if (threadIdx.x == 0) {
+            ptx::prefetch_tensormap(&p.dense.tma_a);
+            ptx::prefetch_tensormap(&p.dense.tma_b);
+            ptx::prefetch_tensormap(&p.dense.tma_c);
+        }
+    }
+    ptx::tc_fence_before_sync();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_TMEM_SLOT);
+
+    if (warp == 0) {
+        // ================================ TMA producer ================================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int g = 0, g_fenced = -1;
+            int64_t issued = 0;          // k-blocks whose loads this thread issued
+            bool aborted = false;
+            bool withhold = (p.withhold_kb >= 0) && blockIdx.x == 0;
+            for (int64_t t = unit; t < p.total_tiles && !aborted; t += num_units) {
+                g = find_problem<Cfg>(p, t, g);
+                const Problem& pr = problem_of<Cfg>(p, g);
+                if constexpr (Cfg::GROUPED) {
+                    if (g != g_fenced) {
+                        ptx::fence_tensormap_acquire(&pr.tma_a);
+                        ptx::fence_tensormap_acquire(&pr.tma_b);
+                        g_fenced = g;
+                    }
+                }
+                const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
+                const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;
+                for (int kb = 0; kb < pr.k_blocks; ++kb) {
+                    if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, t, stage)) {
+                        aborted = true;
+                        break;
+                    }
+                    const bool skip = withhold && kb == p.withhold_kb;
+                    if (!skip) {
+                        const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES * CG);
+                        const int k0 = kb * BK;
+                        const uint32_t a_dst = sA + stage * Cfg::A_BYTES;
+                        const uint32_t b_dst = sB + stage * Cfg::B_BYTES;
+                        auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
+                            if constexpr (CG == 2) ptx::tma_load_2d_pair(dst, m, x, y, fb);
+                            else ptx::tma_load_2d(dst, m, x, y, fb);
+                        };
+                        if constexpr (Cfg::A_MN) {
+                            load(a_dst, &pr.tma_a, tc.m0, k0);
+                            load(a_dst + 8192, &pr.tma_a, tc.m0 + 64, k0);
+                        } else {
+                            load(a_dst, &pr.tma_a, k0, tc.m0);
+                        }
+                        if constexpr (Cfg::B_MN) {
+#pragma unroll
+                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+                        } else {
+                            load(b_dst, &pr.tma_b, k0, nb0);
+                        }
+                        ++issued;
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                withhold = false;
+            }
+            if (!aborted) {
+                // Tail: wait until the MMA has released every slot, so no commit
+                // arrives on this CTA's barriers after it leaves.
+                for (int i = 0; i < STAGES; ++i) {
+                    if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, -1, stage)) {
+                        aborted = true;
+                        break;
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (aborted && issued > 0) {
+                // Loads already issued still land in this CTA's shared memory:
+                // give them time (they complete without any consumer).
+                sleep_ns(200000);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================ MMA issuer ================================
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int g = 0;
+            bool aborted = false;
+            bool any_mma = false;
+            for (int64_t t = unit; t < p.total_tiles && !aborted; t += num_units) {
+                g = find_problem<Cfg>(p, t, g);
+                const Problem& pr = problem_of<Cfg>(p, g);
+                if (!wait_bounded<CG>(tempty_bar(acc), acc_phase ^ 1u, p, abort_addr, ROLE_MMA, t, 16 + acc)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < pr.k_blocks; ++kb) {
+                    if (!wait_bounded<CG>(full_bar(stage), phase, p, abort_addr, ROLE_MMA, t, stage)) {
+                        aborted = true;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t a_addr = sA + stage * Cfg::A_BYTES;
+                    const uint32_t b_addr = sB + stage * Cfg::B_BYTES;
+                    const uint64_t a_desc = Cfg::A_MN ? ptx::smem_desc_sw128(a_addr, 8192, 1024)
+                                                      : ptx::smem_desc_sw128(a_addr, 16, 1024);
+                    const uint64_t b_desc = Cfg::B_MN ? ptx::smem_desc_sw128(b_addr, 8192, 1024)
+                                                      : ptx::smem_desc_sw128(b_addr, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // K-major: the next 16 K elements are 32 bytes further along the
+                        // swizzled row; MN-major: 16 rows (2048 bytes) further down.
+                        const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
+                        const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
+                        ptx::mma_bf16<CG>(d_tmem, a_desc + a_off, b_desc + b_off, Cfg::IDESC,
+                                          (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    any_mma = true;
+                    if constexpr (CG == 2) ptx::mma_commit_pair(empty_bar(stage), 0x3);
+                    else ptx::mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (aborted) break;
+                if (pr.k_blocks > 0) {
+                    if constexpr (CG == 2) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
+                    else ptx::mma_commit(tfull_bar(acc));
+                } else {
+                    // K == 0: nothing to accumulate; the epilogue writes epilogue(0).
+                    ptx::mbar_arrive(tfull_bar(acc));
+                    if constexpr (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa(tfull_bar(acc), 1));
+                }
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            if (aborted && any_mma) {
+                // Drain: one more commit completes when every MMA issued so far has.
+                if constexpr (CG == 2) ptx::mma_commit_pair(drain_bar, 0x1);
+                else ptx::mma_commit(drain_bar);
+                if (!wait_quiet(drain_bar, 0, p.wait_budget_ns)) report_timeout(p, ROLE_DRAIN, -1, 0, p.wait_budget_ns);
+            }
+        }
+    } else {
+        // ================================ epilogue ================================
+        const int ew = warp - EPI_WARP0;                     // 0..3
+        const int q = warp % 4;                              // TMEM lane quarter this warp may read
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        __nv_bfloat16* bias_s = reinterpret_cast<__nv_bfloat16*>(smem + Cfg::OFF_BIAS) + ew * BN;
+        const uint32_t c_stage0 = sC + ew * 2 * C_STAGE_BYTES;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int sbuf = 0;
+        int g = 0, g_fenced = -1;
+        for (int64_t t = unit; t < p.total_tiles; t += num_units) {
+            g = find_problem<Cfg>(p, t, g);
+            const Problem& pr = problem_of<Cfg>(p, g);
+            if constexpr (Cfg::GROUPED) {
+                if (lane == 0 && g != g_fenced) {
+                    ptx::fence_tensormap_acquire(&pr.tma_c);
+                    g_fenced = g;
+                }
+            }
+            const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
+            const int row0 = tc.m0 + q * 32;
+            const bool active = row0 < pr.M;
+            const int epi = pr.epi;
+
+            // bias of this tile's columns into this warp's slot (zeros past N)
+            if (epi != EPI_NONE && active) {
+                for (int i = lane; i < BN; i += 32) {
+                    const int n = tc.n0 + i;
+                    bias_s[i] = (n < pr.N) ? pr.bias[n] : __float2bfloat16_rn(0.0f);
+                }
+            }
+
+            uint32_t ok = 1;
+            if (lane == 0) ok = wait_bounded<CG>(tfull_bar(acc), acc_phase, p, abort_addr, ROLE_EPILOGUE, t, 16 + acc) ? 1u : 0u;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ptx::tc_fence_after_sync();
+            __syncwarp();
+
+            const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
+            constexpr int CHUNKS = BN / Cfg::CW;
+#pragma unroll 1
+            for (int c = 0; c < CHUNKS; ++c) {
+                float v[Cfg::CW];
+                if (pr.k_blocks > 0 && active) {
+                    uint32_t r[32];
+#pragma unroll
+                    for (int h = 0; h < Cfg::CW / 32; ++h) {
+                        ptx::tmem_ld_32x32b_x32(t_acc + c * Cfg::CW + h * 32, r);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(r[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < Cfg::CW; ++i) v[i] = 0.0f;
+                }
+                if (c == CHUNKS - 1) {
+                    // accumulator buffer fully read: hand it back to the MMA issuer
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (CG == 2 && !leader) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
+                        else ptx::mbar_arrive(tempty_bar(acc));
+                    }
+                }
+                const int n_chunk = tc.n0 + c * Cfg::CW;
+                if (!active || n_chunk >= pr.N) continue;
+
+                if (epi != EPI_NONE) {
+                    const __nv_bfloat16* bs = bias_s + c * Cfg::CW;
+#pragma unroll
+                    for (int i = 0; i < Cfg::CW; ++i) v[i] += __bfloat162float(bs[i]);
+                    if (epi == EPI_BIAS_GELU) {
+#pragma unroll
+                        for (int i = 0; i < Cfg::CW; ++i) v[i] = gelu_tanh_f32(v[i]);
+                    }
+                }
+
+                // stage: this lane's row (128 bytes) as eight 16-byte chunks, 128-byte swizzled
+                const uint32_t buf = c_stage0 + sbuf * C_STAGE_BYTES;
+                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                __syncwarp();
+                const uint32_t row_addr = buf + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t w0, w1, w2, w3;
+                    if constexpr (Cfg::C_F32) {
+                        w0 = __float_as_uint(v[4 * j + 0]);
+                        w1 = __float_as_uint(v[4 * j + 1]);
+                        w2 = __float_as_uint(v[4 * j + 2]);
+                        w3 = __float_as_uint(v[4 * j + 3]);
+                    } else {
+                        w0 = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+                        w1 = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+                        w2 = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+                        w3 = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+                    }
+                    const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                                 :: "r"(dst), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(&pr.tma_c, buf, n_chunk, row0);
+                    ptx::bulk_commit_group();
+                }
+                sbuf ^= 1;
+            }
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ---- teardown (lanes 1-31 of warps 0 and 1 wait here for their lane 0)
+    __syncwarp();
+    ptx::tc_fence_before_sync();
+    if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
+    ptx::tc_fence_after_sync();
+    if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
+}
+
+}  // namespace tg

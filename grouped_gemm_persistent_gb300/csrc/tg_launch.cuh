@@ -1,0 +1,33 @@
+// tg_launch.cuh - launch interface between the host API and the kernel
+// instantiations.  The kernel template is instantiated only in tg_inst.cu
+// (compiled once per (grouped, output dtype) pair so the variants build in
+// parallel); the host API sees these declarations only.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "tg_kernel.cuh"
+
+namespace tg {
+
+// Enqueue one persistent launch of gemm_kernel<Cfg> with `grid` CTAs.
+template <class Cfg>
+cudaError_t launch(const Params& p, int grid, cudaStream_t stream);
+
+// How many work units (CTAs, or CTA pairs) of gemm_kernel<Cfg> can be resident
+// at once on the current device.
+template <class Cfg>
+cudaError_t resident_units(int* units);
+
+}  // namespace tg
+
+// Every (BN, CTA_GROUP, A_MN, B_MN) combination for one (C_F32, GROUPED) pair.
+#define TG_FOR_EACH_TILE(X, C_F32, GROUPED)          \
+    X(128, 1, false, false, C_F32, GROUPED)          \
+    X(128, 1, false, true, C_F32, GROUPED)           \
+    X(128, 1, true, false, C_F32, GROUPED)           \
+    X(128, 1, true, true, C_F32, GROUPED)            \
+    X(256, 1, false, false, C_F32, GROUPED)          \
+    X(256, 1, false, true, C_F32, GROUPED)           \
+    X(256, 1, true, false, C_F32, GROUPED)           \
+    X(256, 1, true, true, C_F32, GROUPED)

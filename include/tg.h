@@ -1,0 +1,174 @@
+/*
+ * tg.h - C ABI of libtg: bf16 GEMM and grouped GEMM on NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  C = epilogue(A . B) with bf16 operands, an fp32
+ * accumulator summed over K in BLOCK_K steps, and an epilogue fused into the
+ * same kernel: none, + bias, or + bias then GELU(tanh).  This is the tiled
+ * matmul that "How We Built TLX: A Hardware-Native GPU Compiler for Production
+ * ML at Scale" uses as its running example (section "Introducing TLX": the
+ * standard Triton listing fixes the arithmetic, the TLX-on-Blackwell listing
+ * the producer / MMA / epilogue split), with the bias + GELU fusion of the
+ * TileGym/cuTile tutorial page.  The grouped form is the MoE expert GEMM of
+ * the same TLX article's third case study ("Distributed grouped GEMM for LLM
+ * pre-training"): one problem per expert, ragged M, one persistent launch.
+ *
+ * Where it runs.  One persistent, warp-specialised CUDA kernel on the
+ * current device: a TMA producer warp fills a shared-memory ring guarded by
+ * mbarriers, one thread issues tcgen05.mma into TMEM accumulators (double
+ * buffered), four epilogue warps drain TMEM, apply the epilogue and store C
+ * with TMA.  There is no CPU fallback and no other backend: on a device that
+ * is not sm_103 every compute call fails with TG_ERR_UNSUPPORTED.
+ *
+ * Conventions for every entry point below.
+ *  - All matrix pointers are DEVICE pointers owned by the caller; the library
+ *    never frees, keeps or reallocates them.  Calls are asynchronous on
+ *    `stream` (NULL = the legacy default stream) and return after enqueue;
+ *    the caller keeps A, B, C and bias alive until the stream has run.
+ *  - Arguments are checked on the host before anything is enqueued; a call
+ *    that returns an error has launched nothing.  tg_last_error_message()
+ *    describes the most recent failure on the calling thread.
+ *  - TMA addressing rules: every matrix base pointer must be 16-byte aligned
+ *    and every leading dimension * element size a multiple of 16 bytes
+ *    (bf16: ld % 8 == 0; fp32: ld % 4 == 0).  M, N, K and leading dimensions
+ *    must be below 2^31.  Breaking these gives TG_ERR_UNSUPPORTED.
+ *  - Degenerate sizes: M == 0 or N == 0 is a no-op returning TG_OK.  K == 0
+ *    is the empty sum: C = epilogue(0), i.e. zeros, bias, or GELU(bias).
+ *  - Results are deterministic: no split-K, no atomics; two identical calls
+ *    write bitwise-identical C.
+ */
+#ifndef TG_H
+#define TG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL selects the legacy default stream. */
+typedef struct CUstream_st *tg_stream_t;
+
+typedef enum {
+    TG_OK = 0,
+    TG_ERR_INVALID_ARG = 1,  /* null pointer, negative size, ld too small, bad enum */
+    TG_ERR_UNSUPPORTED = 2,  /* alignment / size limits, or the device is not sm_103 */
+    TG_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed (message has the CUDA error) */
+    TG_ERR_TIMEOUT = 4,      /* a bounded in-kernel wait ran out (reported by tg_device_status) */
+    TG_ERR_NO_DEVICE = 5     /* no CUDA device / driver is available */
+} tg_status;
+
+typedef enum {
+    TG_EPI_NONE = 0,       /* C = A.B */
+    TG_EPI_BIAS = 1,       /* C = A.B + bias[j] */
+    TG_EPI_BIAS_GELU = 2   /* C = gelu_tanh(A.B + bias[j]), gelu_tanh(z) = z/2 (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3))) */
+} tg_epilogue;
+
+typedef enum {
+    TG_ROW_MAJOR = 0,  /* element (r, c) at p[r * ld + c] */
+    TG_COL_MAJOR = 1   /* element (r, c) at p[c * ld + r] */
+} tg_layout;
+
+typedef enum {
+    TG_BF16 = 0,  /* output rounded once, to nearest even, from the fp32 epilogue value */
+    TG_F32 = 1    /* output is the fp32 epilogue value itself */
+} tg_dtype;
+
+/*
+ * tg_gemm - one dense GEMM, C[M,N] = epilogue(A[M,K] . B[K,N]).
+ *
+ *   A, layout_a, lda : bf16 M x K.  Row-major: lda >= K.  Column-major: lda >= M.
+ *   B, layout_b, ldb : bf16 K x N.  Row-major: ldb >= N.  Column-major (i.e. the
+ *                      N x K matrix B^T stored row-major): ldb >= K.
+ *   C, c_dtype, ldc  : M x N, always row-major, ldc >= N, bf16 or fp32.
+ *   epi, bias        : bias is a device bf16[N] (2-byte aligned); required for
+ *                      TG_EPI_BIAS / TG_EPI_BIAS_GELU, ignored for TG_EPI_NONE.
+ *   A and B may be NULL only when K == 0.  C must not overlap A, B or bias.
+ *
+ * Accumulation is fp32 in tensor memory; the epilogue runs in fp32 and rounds
+ * once.  Each element agrees with the exact result within
+ * 1e-2 * sum_k |a_ik b_kj| (+ 1e-2 |bias_j|) + 1e-5.
+ */
+tg_status tg_gemm(const void *A, tg_layout layout_a, int64_t lda,
+                  const void *B, tg_layout layout_b, int64_t ldb,
+                  void *C, tg_dtype c_dtype, int64_t ldc,
+                  int64_t M, int64_t N, int64_t K,
+                  tg_epilogue epi, const void *bias,
+                  tg_stream_t stream);
+
+/*
+ * One problem of a grouped GEMM: C_g = epilogue_g(A_g . B_g), fields as in
+ * tg_gemm.  Problems are independent and may differ in every field; a problem
+ * with M == 0 or N == 0 (an expert that received no tokens) is skipped and its
+ * pointers may be NULL.
+ */
+typedef struct tg_group_problem {
+    int64_t M, N, K;
+    const void *A;  int64_t lda; tg_layout layout_a;
+    const void *B;  int64_t ldb; tg_layout layout_b;
+    void *C;        int64_t ldc; tg_dtype c_dtype;
+    tg_epilogue epi;
+    const void *bias;
+} tg_group_problem;
+
+/*
+ * tg_grouped_gemm - G independent GEMMs in one persistent launch (one launch
+ * per distinct (layout_a, layout_b, c_dtype) combination present).
+ *
+ *   table : HOST array of G problems.  It is read during the call and may be
+ *           reused or freed as soon as the call returns.
+ *   G     : number of problems, 0 <= G <= 65536.  G == 0 is a no-op.
+ *
+ * The persistent tile scheduler walks the output tiles of all non-empty
+ * problems in table order (prefix sums of per-problem tile counts).  The
+ * library encodes per-problem TMA descriptors on the host and copies them into
+ * a stream-ordered device workspace that it allocates and frees on `stream`
+ * (from a library-owned memory pool); nothing outlives the launch.
+ * Errors are as for tg_gemm; a bad problem g is named in the message.
+ */
+tg_status tg_grouped_gemm(const tg_group_problem *table, int G, tg_stream_t stream);
+
+/* Static English description of a status code (never NULL). */
+const char *tg_status_string(tg_status status);
+
+/*
+ * Description of the most recent failing call on the calling thread (argument
+ * check, CUDA error or in-kernel timeout, with the offending value or problem
+ * index).  Owned by the library, valid until the thread's next libtg call.
+ */
+const char *tg_last_error_message(void);
+
+/*
+ * tg_device_status - synchronise `stream`, then read and clear the current
+ * device's error record.  Returns TG_OK, TG_ERR_CUDA (the stream reported a
+ * CUDA error), or TG_ERR_TIMEOUT (a kernel's bounded mbarrier wait ran out:
+ * the kernel recorded the role, tile and stage, stopped, drained its own
+ * in-flight copies and MMAs, freed its tensor memory and returned; the context
+ * stays usable).  The record is per device and shared by all streams.
+ */
+tg_status tg_device_status(tg_stream_t stream);
+
+/*
+ * Wait budget of every in-kernel mbarrier wait, in milliseconds (default 1000,
+ * or the TG_WAIT_BUDGET_MS environment variable read at the first call).
+ * Applies to launches made after the call.  0 restores the default.
+ */
+tg_status tg_set_wait_budget_ms(uint32_t ms);
+
+/*
+ * Test hook for the failure path.  The next launch made by this thread has
+ * its TMA producer withhold the arrival for the k-block with global index
+ * `k_block` of its first tile, so the MMA issuer's bounded wait on that stage
+ * runs out and tg_device_status reports TG_ERR_TIMEOUT.  -1 (the default)
+ * disables it; the hook disarms itself after one launch.  Nothing faults.
+ */
+tg_status tg_debug_withhold_stage(int64_t k_block);
+
+/* Library version as (major << 16) | minor. */
+uint32_t tg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_H */

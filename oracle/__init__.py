@@ -182,7 +182,7 @@ def compare(c: np.ndarray, y: np.ndarray, s: np.ndarray, bias_abs: np.ndarray | 
     """Element-wise check of a computed C against the oracle.
 
     Returns a dict: ok, max_abs_err, max_ratio (err / bound), n_bad, worst
-    index, and the tight diagnostic max err / (2^-8 |y| + 2^-11 S) that flags
+    index, and the tight diagnostic max err / (2^-8 |y| + 2^-11 (S + |bias|)) that flags
     dropped or repeated K-slices the loose bound can miss.
     """
     c = np.asarray(c, dtype=np.float64)
@@ -190,7 +190,8 @@ def compare(c: np.ndarray, y: np.ndarray, s: np.ndarray, bias_abs: np.ndarray | 
     bnd = bound(s, bias_abs)
     bad = ~(err <= bnd)  # NaN counts as bad
     ratio = err / bnd
-    tight = err / (2.0 ** -8 * np.abs(y) + 2.0 ** -11 * s + 1e-30)
+    scale = s if bias_abs is None else s + bias_abs[None, :]
+    tight = err / (2.0 ** -8 * np.abs(y) + 2.0 ** -11 * scale + 1e-30)
     worst = np.unravel_index(np.nanargmax(ratio), ratio.shape) if ratio.size else None
     return {
         "ok": bool(not bad.any()),

@@ -1,0 +1,315 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Every test compares element by element on seeded inputs, within
+|err| <= 1e-2 * sum_k |a_ik b_kj| (+ 1e-2 |bias_j|) + 1e-5, and also checks the
+tight diagnostic that catches dropped or repeated K-slices.  Where the exact
+result is an integer below 2^24 the comparison is bitwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+import grouped_gemm_persistent_gb300 as tg
+import oracle
+from grouped_gemm_persistent_gb300 import workloads as wl
+
+from parity import check_dense, oracle_dense, run_dense, sample_rows, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = [(False, False), (False, True), (True, False), (True, True)]   # (A column-major, B column-major)
+
+
+def pad8(x: int) -> int:
+    """Leading dimensions are padded to 8 bf16 elements (TMA: row strides are multiples of 16 bytes)."""
+    return -(-x // 8) * 8
+
+
+def lds(M, N, K, a_col, b_col):
+    return dict(lda=pad8(M if a_col else K), ldb=pad8(K if b_col else N))
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _built():
+    from grouped_gemm_persistent_gb300.build import build
+    build()
+    tg.load()
+
+
+def _sync_ok():
+    tg.device_status()
+
+
+# ------------------------------------------------------------------------------------------ dense
+
+def test_dense_256_workload():
+    case = wl.dense_case("dense_256")
+    c = run_dense(case)
+    _sync_ok()
+    check_dense(case, c)
+
+
+@pytest.mark.parametrize("a_col,b_col", LAYOUTS)
+@pytest.mark.parametrize("epi", ["none", "bias", "bias_gelu"])
+@pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
+def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype):
+    # spans several tiles with a ragged tail in M, N and K (K not a multiple of 64)
+    case = wl.dense_random(333, 392, 200, seed=100, dist="uniform", a_col_major=a_col, b_col_major=b_col,
+                           epi=epi, c_dtype=c_dtype, **lds(333, 392, 200, a_col, b_col))
+    c = run_dense(case)
+    _sync_ok()
+    check_dense(case, c)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (1, 8, 8), (129, 264, 65), (512, 256, 1024), (17, 16, 3000),
+                                   (640, 136, 128), (7, 520, 72)])
+@pytest.mark.parametrize("a_col,b_col", [(False, False), (False, True)])
+def test_dense_shapes(M, N, K, a_col, b_col):
+    case = wl.dense_random(M, N, K, seed=M * 7 + N * 3 + K, dist="normal", a_col_major=a_col, b_col_major=b_col,
+                           epi="bias", c_dtype="bf16", **lds(M, N, K, a_col, b_col))
+    c = run_dense(case)
+    _sync_ok()
+    check_dense(case, c)
+
+
+def test_padded_leading_dimensions():
+    case = wl.dense_random(200, 136, 150, seed=9, dist="normal", lda=160, ldb=144, epi="bias_gelu")
+    c_full = torch.full((200, 152), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = c_full[:, :136]
+    run_dense(case, out)
+    _sync_ok()
+    check_dense(case, out)
+    assert torch.isnan(c_full[:, 136:].float()).all(), "columns beyond N were written"
+
+
+def test_integer_exact_bitwise():
+    # integers in [-4, 4]: every fp32 partial sum is exact, so C must equal the
+    # exact result bit for bit (fp32 out) and its RNE rounding (bf16 out)
+    for a_col, b_col in LAYOUTS:
+        case = wl.dense_random(300, 264, 640, seed=5, dist="int4", a_col_major=a_col, b_col_major=b_col,
+                               c_dtype="f32", **lds(300, 264, 640, a_col, b_col))
+        y, _ = oracle_dense(case)
+        c = run_dense(case)
+        _sync_ok()
+        assert np.array_equal(to_f64(c), y), f"fp32 output not exact for layouts {a_col, b_col}"
+        case.c_dtype = "bf16"
+        c16 = run_dense(case)
+        _sync_ok()
+        want = torch.from_numpy(y).to(torch.bfloat16)
+        assert torch.equal(c16.cpu().view(torch.int16), want.view(torch.int16))
+
+
+def test_identity_and_permutation_exact():
+    M, N = 256, 192
+    rng = np.random.default_rng(1)
+    perm = rng.permutation(M)
+    P = torch.zeros((M, M), dtype=torch.bfloat16)
+    P[torch.arange(M), torch.from_numpy(perm)] = 1
+    B = torch.randn((M, N), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16)
+    c = tg.gemm(P.cuda(), B.cuda(), out_dtype=torch.float32)
+    _sync_ok()
+    assert torch.equal(c.cpu(), B.float()[torch.from_numpy(perm)])
+    # B = I: C = A; column-major B view
+    A = torch.randn((M, 128), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    eye = torch.eye(128, dtype=torch.bfloat16).cuda()
+    c = tg.gemm(A.cuda(), eye.t().contiguous().t(), out_dtype=torch.float32)
+    _sync_ok()
+    assert torch.equal(c.cpu(), A.float())
+
+
+def test_k_zero_is_epilogue_of_zero():
+    M, N = 130, 200
+    bias = (torch.randn(N, generator=torch.Generator().manual_seed(4)) * 3).to(torch.bfloat16)
+    a = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty((0, N), dtype=torch.bfloat16, device="cuda")
+    for epi in ("none", "bias", "bias_gelu"):
+        c = tg.gemm(a, b, bias=bias.cuda(), epilogue=epi, out_dtype=torch.float32)
+        _sync_ok()
+        z = torch.zeros((M, N), dtype=torch.float64) + (bias.double() if epi != "none" else 0)
+        want = torch.nn.functional.gelu(z, approximate="tanh") if epi == "bias_gelu" else z
+        assert torch.allclose(c.cpu().double(), want, rtol=2e-3, atol=1e-5), epi
+
+
+def test_empty_m_or_n_writes_nothing():
+    a = torch.randn((0, 64), device="cuda").to(torch.bfloat16)
+    b = torch.randn((64, 64), device="cuda").to(torch.bfloat16)
+    out = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    tg.gemm(a, b, out)
+    _sync_ok()
+
+
+def test_guard_bands_untouched():
+    case = wl.dense_random(300, 264, 128, seed=12, dist="normal", epi="bias")
+    big = torch.full((300 + 64, 264 + 40), float("inf"), dtype=torch.float32, device="cuda")
+    out = big[32:332, 8:272]
+    run_dense(wl.dense_random(300, 264, 128, seed=12, dist="normal", epi="bias", c_dtype="f32"), out)
+    _sync_ok()
+    case.c_dtype = "f32"
+    check_dense(case, out)
+    mask = torch.ones_like(big, dtype=torch.bool)
+    mask[32:332, 8:272] = False
+    assert torch.isinf(big[mask]).all(), "a write landed outside C"
+
+
+def test_deterministic_bitwise():
+    case = wl.dense_random(1000, 1000, 1000, seed=13, dist="normal", epi="bias_gelu")
+    c1 = run_dense(case)
+    c2 = run_dense(case)
+    _sync_ok()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+
+
+def test_nan_stays_in_its_row():
+    case = wl.dense_random(256, 256, 256, seed=14, dist="normal", c_dtype="f32")
+    case.a = case.a.clone()
+    case.a[37, 11] = float("nan")
+    c = run_dense(case).cpu()
+    _sync_ok()
+    assert torch.isnan(c[37]).all()
+    rest = torch.cat([c[:37], c[38:]])
+    assert torch.isfinite(rest).all()
+
+
+def test_side_stream():
+    case = wl.dense_random(512, 512, 512, seed=15, dist="normal")
+    a, b = case.a.cuda(), case.b.cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        c = tg.gemm(a, b, stream=s)
+    tg.device_status(s)
+    check_dense(case, c)
+
+
+# ------------------------------------------------------------------------------------------ grouped
+
+def _grouped_problems(counts, N, K, seed, epi="none", c_dtype="bf16", b_col=False):
+    case = wl.grouped_random(counts, N, K, seed, epi=epi, c_dtype=c_dtype)
+    a = case.a.cuda()
+    bst = case.b if not b_col else case.b.transpose(1, 2).contiguous()   # [G, N, K] storage if col-major
+    b = bst.cuda()
+    dt = torch.float32 if c_dtype == "f32" else torch.bfloat16
+    out = torch.empty((int(np.sum(counts)), N), dtype=dt, device="cuda")
+    bias = case.bias.cuda() if case.bias is not None else None
+    return case, a, b, out, bias
+
+
+def _check_grouped(case, out, b_col=False, rows_per_group=None):
+    c_all = out.float().cpu().double().numpy()
+    for g in range(case.G):
+        r0, r1 = case.offsets[g], case.offsets[g + 1]
+        if r1 == r0:
+            continue
+        a_g = wl.bf16_bits(case.a[r0:r1])
+        b_g = wl.bf16_bits(case.b[g] if not b_col else case.b[g].t().contiguous())
+        bias = wl.bf16_bits(case.bias[g]) if case.bias is not None else None
+        rows = None if rows_per_group is None else rows_per_group[g]
+        y, s = oracle.gemm(a_g, b_g, b_col_major=b_col, bias=bias, epi=case.epi, rows=rows)
+        c = c_all[r0:r1] if rows is None else c_all[r0 + rows]
+        bias_abs = np.abs(case.bias[g].double().numpy()) if case.bias is not None else None
+        r = oracle.compare(c, y, s, bias_abs)
+        assert r["ok"] and r["max_tight"] < 4.0, f"group {g}: {r}"
+
+
+@pytest.mark.parametrize("epi", ["none", "bias_gelu"])
+@pytest.mark.parametrize("b_col", [False, True])
+def test_grouped_ragged_with_empty_groups(epi, b_col):
+    counts = [0, 300, 5, 0, 130, 257, 1, 0]        # empty first, middle and last
+    case, a, b, out, bias = _grouped_problems(counts, 136, 200, 21, epi=epi, b_col=b_col)
+    sentinel = torch.full_like(out, float("nan"))
+    out.copy_(sentinel)
+    bview = b.transpose(1, 2) if b_col else b      # logical [G, K, N]
+    tg.moe_grouped_gemm(a, bview, counts, out, bias=bias, epilogue=epi)
+    _sync_ok()
+    assert not torch.isnan(out.float()).any(), "a row of a non-empty group was not written"
+    _check_grouped(case, out, b_col=b_col)
+
+
+def test_grouped_single_group_matches_dense_bitwise():
+    case = wl.dense_random(700, 392, 320, seed=22, dist="normal", epi="bias")
+    a, b, bias = case.a.cuda(), case.b.cuda(), case.bias.cuda()
+    dense = tg.gemm(a, b, bias=bias, epilogue="bias")
+    grouped = tg.moe_grouped_gemm(a, b[None], [700], bias=bias[None], epilogue="bias")
+    _sync_ok()
+    assert torch.equal(dense.view(torch.int16), grouped.view(torch.int16))
+
+
+def test_grouped_mixed_layouts_and_dtypes():
+    # problems of different layouts and output types in one call (one launch per class)
+    gen = torch.Generator().manual_seed(23)
+    probs, refs = [], []
+    specs = [(100, 136, 64, False, False, "bf16"), (260, 128, 200, False, True, "f32"),
+             (0, 128, 64, False, False, "bf16"), (40, 264, 72, True, False, "bf16"),
+             (129, 136, 128, False, False, "f32")]
+    keep = []
+    for (M, N, K, a_col, b_col, cd) in specs:
+        a = (torch.randn((K, M) if a_col else (M, K), generator=gen) / 8).to(torch.bfloat16)
+        b = (torch.randn((N, K) if b_col else (K, N), generator=gen) / 8).to(torch.bfloat16)
+        da, db = a.cuda(), b.cuda()
+        out = torch.empty((M, N), dtype=torch.float32 if cd == "f32" else torch.bfloat16, device="cuda")
+        keep += [da, db, out]
+        probs.append(tg.make_problem(da.t() if a_col else da, db.t() if b_col else db, out))
+        refs.append((a, b, a_col, b_col, out))
+    tg.grouped_gemm_table(probs)
+    _sync_ok()
+    for a, b, a_col, b_col, out in refs:
+        if out.shape[0] == 0:
+            continue
+        y, s = oracle.gemm(wl.bf16_bits(a), wl.bf16_bits(b), a_col_major=a_col, b_col_major=b_col)
+        r = oracle.compare(to_f64(out), y, s)
+        assert r["ok"] and r["max_tight"] < 4.0, r
+
+
+# ------------------------------------------------------------------------------------------ failure path
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    case = wl.dense_random(256, 256, 512, seed=30, dist="normal")
+    a, b = case.a.cuda(), case.b.cuda()
+    tg.set_wait_budget_ms(100)
+    try:
+        tg.debug_withhold_stage(3)           # the first CTA never gets k-block 3 of its first tile
+        tg.gemm(a, b)
+        with pytest.raises(tg.TGError) as ei:
+            tg.device_status()
+        assert ei.value.status == tg.TG_ERR_TIMEOUT
+        assert "role=" in str(ei.value)
+    finally:
+        tg.set_wait_budget_ms(0)
+    # the context is still usable and the record was cleared
+    c = run_dense(case)
+    _sync_ok()
+    check_dense(case, c)
+
+
+# ------------------------------------------------------------------------------------------ full-size workloads
+
+def test_workload_dense_4096_bias_gelu_full():
+    case = wl.dense_case("dense_4096_bias_gelu")
+    c = run_dense(case)
+    _sync_ok()
+    check_dense(case, c)
+
+
+def test_workload_dense_8192_f32_sampled():
+    case = wl.dense_case("dense_8192_f32")
+    c = run_dense(case)
+    _sync_ok()
+    rows = sample_rows(case.M, 256, 192, seed=1)
+    check_dense(case, c, rows=rows)
+
+
+def test_workload_skinny_bcast_full():
+    case = wl.dense_case("skinny_bcast")
+    c = run_dense(case)
+    _sync_ok()
+    check_dense(case, c)
+
+
+def test_workload_grouped_moe_sampled():
+    case = wl.grouped_case("grouped_moe")
+    a, b = case.a.cuda(), case.b.cuda()
+    out = torch.full((a.shape[0], case.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tg.moe_grouped_gemm(a, b, case.counts, out)
+    _sync_ok()
+    assert not torch.isnan(out.float()).any()
+    rows = [sample_rows(int(m), 256, 24, seed=g) if m else np.zeros(0, np.int64) for g, m in enumerate(case.counts)]
+    _check_grouped(case, out, rows_per_group=rows)
