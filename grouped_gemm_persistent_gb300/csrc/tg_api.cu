@@ -76,7 +76,7 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0, sms = 0;
     tg::ErrorRecord* err = nullptr;
     cudaMemPool_t pool = nullptr;
-    int units[64] = {};   // resident work units per kernel variant (0 = not yet queried)
+    int units[128] = {};  // resident work units per kernel variant (0 = not yet queried)
 };
 
 std::mutex g_mu;
@@ -227,10 +227,12 @@ const Variant kVariants[] = {
     TG_FOR_EACH_TILE(TG_VARIANT_ENTRY, false, true)
     TG_FOR_EACH_TILE(TG_VARIANT_ENTRY, true, true)
 };
-constexpr int kTilesPerGroup = 8;
+constexpr int kTilesPerGroup = 16;
+constexpr int kNumVariants = 4 * kTilesPerGroup;
+static_assert(sizeof(kVariants) / sizeof(kVariants[0]) == kNumVariants, "variant table");
 
-int variant_index(bool grouped, bool f32, int bn, bool amn, bool bmn) {
-    const int tile = (bn == 256 ? 4 : 0) + (amn ? 2 : 0) + (bmn ? 1 : 0);
+int variant_index(bool grouped, bool f32, int cta_group, int bn, bool amn, bool bmn) {
+    const int tile = (cta_group == 2 ? 8 : 0) + (bn == 256 ? 4 : 0) + (amn ? 2 : 0) + (bmn ? 1 : 0);
     return ((grouped ? 2 : 0) + (f32 ? 1 : 0)) * kTilesPerGroup + tile;
 }
 
@@ -249,7 +251,30 @@ tg_status resident(DeviceState* d, int vi, int* units) {
     return TG_OK;
 }
 
-int pick_bn(int64_t max_n) { return max_n > 128 ? 256 : 128; }
+struct TileChoice {
+    int cta_group;
+    int bn;
+};
+
+// Tile shape of a launch.  BN = 256 unless every problem is at most 128 wide;
+// CTA pairs (256-row tiles, half the operand traffic per SM) unless the rows
+// are so few that 128-row tiles keep more SMs busy.  TG_TILE=<cta_group>x<bn>
+// (e.g. "2x256") overrides the choice for tuning sweeps.
+TileChoice pick_tile(int64_t rows, int64_t max_n, int sms) {
+    TileChoice t;
+    t.bn = max_n > 128 ? 256 : 128;
+    const int64_t tiles_n = (max_n + t.bn - 1) / t.bn;
+    const int64_t pair_tiles = ((rows + 255) / 256) * tiles_n;
+    t.cta_group = (pair_tiles * 2 >= sms) ? 2 : 1;
+    if (const char* env = std::getenv("TG_TILE")) {
+        int cg = 0, bn = 0;
+        if (std::sscanf(env, "%dx%d", &cg, &bn) == 2 && (cg == 1 || cg == 2) && (bn == 128 || bn == 256)) {
+            t.cta_group = cg;
+            t.bn = bn;
+        }
+    }
+    return t;
+}
 
 // Raster band (N-tiles swept before stepping along M): a square-ish footprint
 // for the tiles that run concurrently, so A rows and B columns are shared in L2.
@@ -324,8 +349,9 @@ tg_status tg_gemm(const void* A, tg_layout layout_a, int64_t lda, const void* B,
     if ((s = device_state(&d)) != TG_OK) return s;
     if ((s = encoder()) != TG_OK) return s;
 
-    const int bn = pick_bn(N);
-    const int vi = variant_index(false, c_dtype == TG_F32, bn, layout_a == TG_COL_MAJOR, layout_b == TG_ROW_MAJOR);
+    const TileChoice tc = pick_tile(M, N, d->sms);
+    const int vi = variant_index(false, c_dtype == TG_F32, tc.cta_group, tc.bn, layout_a == TG_COL_MAJOR,
+                                 layout_b == TG_ROW_MAJOR);
     const Variant& v = kVariants[vi];
     int units = 0;
     if ((s = resident(d, vi, &units)) != TG_OK) return s;
@@ -375,10 +401,14 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
     const int64_t withhold = t_withhold;
     for (const auto& key : order) {
         const std::vector<int>& members = classes[key];
-        int64_t max_n = 0;
-        for (int g : members) max_n = qs[g].N > max_n ? qs[g].N : max_n;
-        const int vi = variant_index(true, std::get<2>(key) == TG_F32, pick_bn(max_n), std::get<0>(key) == TG_COL_MAJOR,
-                                     std::get<1>(key) == TG_ROW_MAJOR);
+        int64_t max_n = 0, rows = 0;
+        for (int g : members) {
+            max_n = qs[g].N > max_n ? qs[g].N : max_n;
+            rows += qs[g].M;
+        }
+        const TileChoice tc = pick_tile(rows, max_n, d->sms);
+        const int vi = variant_index(true, std::get<2>(key) == TG_F32, tc.cta_group, tc.bn,
+                                     std::get<0>(key) == TG_COL_MAJOR, std::get<1>(key) == TG_ROW_MAJOR);
         const Variant& v = kVariants[vi];
         int units = 0;
         if ((s = resident(d, vi, &units)) != TG_OK) return s;

@@ -22,6 +22,7 @@ cudaError_t resident_units(int* units);
 }  // namespace tg
 
 // Every (BN, CTA_GROUP, A_MN, B_MN) combination for one (C_F32, GROUPED) pair.
+// Index within the list: (CTA_GROUP == 2) * 8 + (BN == 256) * 4 + A_MN * 2 + B_MN.
 #define TG_FOR_EACH_TILE(X, C_F32, GROUPED)          \
     X(128, 1, false, false, C_F32, GROUPED)          \
     X(128, 1, false, true, C_F32, GROUPED)           \
@@ -30,4 +31,12 @@ cudaError_t resident_units(int* units);
     X(256, 1, false, false, C_F32, GROUPED)          \
     X(256, 1, false, true, C_F32, GROUPED)           \
     X(256, 1, true, false, C_F32, GROUPED)           \
-    X(256, 1, true, true, C_F32, GROUPED)
+    X(256, 1, true, true, C_F32, GROUPED)            \
+    X(128, 2, false, false, C_F32, GROUPED)          \
+    X(128, 2, false, true, C_F32, GROUPED)           \
+    X(128, 2, true, false, C_F32, GROUPED)           \
+    X(128, 2, true, true, C_F32, GROUPED)            \
+    X(256, 2, false, false, C_F32, GROUPED)          \
+    X(256, 2, false, true, C_F32, GROUPED)           \
+    X(256, 2, true, false, C_F32, GROUPED)           \
+    X(256, 2, true, true, C_F32, GROUPED)

@@ -29,6 +29,16 @@ def lds(M, N, K, a_col, b_col):
     return dict(lda=pad8(M if a_col else K), ldb=pad8(K if b_col else N))
 
 
+TILES = ["1x128", "1x256", "2x128", "2x256"]   # <cta_group>x<BN>: single CTA or CTA pair, tile width
+
+
+@pytest.fixture(params=TILES)
+def tile(request, monkeypatch):
+    """Force one kernel variant (the library reads TG_TILE at every call)."""
+    monkeypatch.setenv("TG_TILE", request.param)
+    return request.param
+
+
 @pytest.fixture(autouse=True, scope="module")
 def _built():
     from grouped_gemm_persistent_gb300.build import build
@@ -52,7 +62,7 @@ def test_dense_256_workload():
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("epi", ["none", "bias", "bias_gelu"])
 @pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
-def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype):
+def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype, tile):
     # spans several tiles with a ragged tail in M, N and K (K not a multiple of 64)
     case = wl.dense_random(333, 392, 200, seed=100, dist="uniform", a_col_major=a_col, b_col_major=b_col,
                            epi=epi, c_dtype=c_dtype, **lds(333, 392, 200, a_col, b_col))
@@ -64,7 +74,7 @@ def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype):
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (1, 8, 8), (129, 264, 65), (512, 256, 1024), (17, 16, 3000),
                                    (640, 136, 128), (7, 520, 72)])
 @pytest.mark.parametrize("a_col,b_col", [(False, False), (False, True)])
-def test_dense_shapes(M, N, K, a_col, b_col):
+def test_dense_shapes(M, N, K, a_col, b_col, tile):
     case = wl.dense_random(M, N, K, seed=M * 7 + N * 3 + K, dist="normal", a_col_major=a_col, b_col_major=b_col,
                            epi="bias", c_dtype="bf16", **lds(M, N, K, a_col, b_col))
     c = run_dense(case)
@@ -82,7 +92,7 @@ def test_padded_leading_dimensions():
     assert torch.isnan(c_full[:, 136:].float()).all(), "columns beyond N were written"
 
 
-def test_integer_exact_bitwise():
+def test_integer_exact_bitwise(tile):
     # integers in [-4, 4]: every fp32 partial sum is exact, so C must equal the
     # exact result bit for bit (fp32 out) and its RNE rounding (bf16 out)
     for a_col, b_col in LAYOUTS:
@@ -99,7 +109,7 @@ def test_integer_exact_bitwise():
         assert torch.equal(c16.cpu().view(torch.int16), want.view(torch.int16))
 
 
-def test_identity_and_permutation_exact():
+def test_identity_and_permutation_exact(tile):
     M, N = 256, 192
     rng = np.random.default_rng(1)
     perm = rng.permutation(M)
@@ -117,7 +127,7 @@ def test_identity_and_permutation_exact():
     assert torch.equal(c.cpu(), A.float())
 
 
-def test_k_zero_is_epilogue_of_zero():
+def test_k_zero_is_epilogue_of_zero(tile):
     M, N = 130, 200
     bias = (torch.randn(N, generator=torch.Generator().manual_seed(4)) * 3).to(torch.bfloat16)
     a = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
@@ -138,7 +148,7 @@ def test_empty_m_or_n_writes_nothing():
     _sync_ok()
 
 
-def test_guard_bands_untouched():
+def test_guard_bands_untouched(tile):
     case = wl.dense_random(300, 264, 128, seed=12, dist="normal", epi="bias")
     big = torch.full((300 + 64, 264 + 40), float("inf"), dtype=torch.float32, device="cuda")
     out = big[32:332, 8:272]
@@ -151,7 +161,7 @@ def test_guard_bands_untouched():
     assert torch.isinf(big[mask]).all(), "a write landed outside C"
 
 
-def test_deterministic_bitwise():
+def test_deterministic_bitwise(tile):
     case = wl.dense_random(1000, 1000, 1000, seed=13, dist="normal", epi="bias_gelu")
     c1 = run_dense(case)
     c2 = run_dense(case)
@@ -212,7 +222,7 @@ def _check_grouped(case, out, b_col=False, rows_per_group=None):
 
 @pytest.mark.parametrize("epi", ["none", "bias_gelu"])
 @pytest.mark.parametrize("b_col", [False, True])
-def test_grouped_ragged_with_empty_groups(epi, b_col):
+def test_grouped_ragged_with_empty_groups(epi, b_col, tile):
     counts = [0, 300, 5, 0, 130, 257, 1, 0]        # empty first, middle and last
     case, a, b, out, bias = _grouped_problems(counts, 136, 200, 21, epi=epi, b_col=b_col)
     sentinel = torch.full_like(out, float("nan"))
@@ -224,7 +234,7 @@ def test_grouped_ragged_with_empty_groups(epi, b_col):
     _check_grouped(case, out, b_col=b_col)
 
 
-def test_grouped_single_group_matches_dense_bitwise():
+def test_grouped_single_group_matches_dense_bitwise(tile):
     case = wl.dense_random(700, 392, 320, seed=22, dist="normal", epi="bias")
     a, b, bias = case.a.cuda(), case.b.cuda(), case.bias.cuda()
     dense = tg.gemm(a, b, bias=bias, epilogue="bias")
@@ -233,7 +243,7 @@ def test_grouped_single_group_matches_dense_bitwise():
     assert torch.equal(dense.view(torch.int16), grouped.view(torch.int16))
 
 
-def test_grouped_mixed_layouts_and_dtypes():
+def test_grouped_mixed_layouts_and_dtypes(tile):
     # problems of different layouts and output types in one call (one launch per class)
     gen = torch.Generator().manual_seed(23)
     probs, refs = [], []
@@ -261,7 +271,7 @@ def test_grouped_mixed_layouts_and_dtypes():
 
 # ------------------------------------------------------------------------------------------ failure path
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+def test_bounded_wait_reports_timeout_and_context_survives(tile):
     case = wl.dense_random(256, 256, 512, seed=30, dist="normal")
     a, b = case.a.cuda(), case.b.cuda()
     tg.set_wait_budget_ms(100)
