@@ -69,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_gemm.argtypes = [vp, ci, i64, vp, ci, i64, vp, ci, i64, i64, i64, i64, ci, vp, vp]
         lib.tg_grouped_gemm.restype = ci
         lib.tg_grouped_gemm.argtypes = [ctypes.POINTER(GroupProblem), ci, vp]
+        lib.tg_grouped_gemm_noalloc.restype = ci
+        lib.tg_grouped_gemm_noalloc.argtypes = [ctypes.POINTER(GroupProblem), ci, vp]
         lib.tg_status_string.restype = ctypes.c_char_p
         lib.tg_status_string.argtypes = [ci]
         lib.tg_last_error_message.restype = ctypes.c_char_p
@@ -169,6 +171,13 @@ def grouped_gemm_table(table, stream=None) -> None:
     """Call tg_grouped_gemm on a sequence of GroupProblem (or a ctypes array of them)."""
     arr = table if isinstance(table, ctypes.Array) else (GroupProblem * len(table))(*table)
     _check(load().tg_grouped_gemm(arr, len(arr), _stream_handle(stream)))
+
+
+def grouped_gemm_table_noalloc(table, stream=None) -> None:
+    """tg_grouped_gemm_noalloc: the same grouped GEMM with its problem table in the
+    library's fixed device array (no device allocation; at most 256 non-empty problems)."""
+    arr = table if isinstance(table, ctypes.Array) else (GroupProblem * len(table))(*table)
+    _check(load().tg_grouped_gemm_noalloc(arr, len(arr), _stream_handle(stream)))
 
 
 def build_moe_table(a: torch.Tensor, b: torch.Tensor, counts, out: torch.Tensor, *, bias: torch.Tensor | None = None,

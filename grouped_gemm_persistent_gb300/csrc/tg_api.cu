@@ -333,6 +333,90 @@ tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t str
 
 }  // namespace
 
+// ----------------------------------------------------------------------------------------
+// Grouped GEMM that allocates nothing (tg_grouped_gemm_noalloc).
+//
+// Some callers may not allocate device memory once they are running: a
+// serving loop that pre-reserves everything at start-up so that no request can
+// fail or stall on an allocation, or an application whose device memory is
+// owned by its own allocator under a fixed budget.  tg_grouped_gemm allocates a
+// small stream-ordered workspace per call for the problem table; this entry
+// point keeps the table in the fixed array below instead.  The array lives in
+// the library's device image, so every GPU that loads libtg holds it (128 KiB)
+// until the process exits.  All calls share it: a call overwrites the entries
+// it uses, and a kernel reads only the entries its own call wrote, so nothing
+// has to start at zero; two calls whose copies and kernels overlap on the GPU
+// (different streams, no ordering between them) race on it.
+
+static __device__ __align__(256) tg::Problem g_noalloc_table[TG_NOALLOC_MAX_PROBLEMS];
+static_assert(sizeof(g_noalloc_table) == 128 * 1024, "the header states a 128 KiB table");
+
+namespace {
+
+struct NoallocDevice {
+    bool ready = false;
+    int sms = 0;
+    tg::ErrorRecord* err = nullptr;
+    tg::Problem* table = nullptr;   // device address of g_noalloc_table on this device
+    int units[128] = {};
+};
+
+NoallocDevice g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: device checks and the device
+// addresses of the scratch table and the error record.  In host code the
+// array's name is only a stand-in for the symbol, so its address on this device
+// comes from cudaGetSymbolAddress.
+tg_status noalloc_device(NoallocDevice** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mu);
+    NoallocDevice& d = g_noalloc[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3)
+            return fail(TG_ERR_UNSUPPORTED, "device %d is sm_%d%d; libtg is built for sm_103a (GB300) only", dev,
+                        major, minor);
+        void* sym = nullptr;
+        if ((e = cudaGetSymbolAddress(&sym, g_tg_error)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(error record)");
+        d.err = static_cast<tg::ErrorRecord*>(sym);
+        tg::Problem* tab = nullptr;
+        if ((e = cudaGetSymbolAddress((void**)&tab, g_noalloc_table)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(no-alloc problem table)");
+        d.table = tab;
+        d.ready = true;
+    }
+    *out = &d;
+    return TG_OK;
+}
+
+tg_status noalloc_resident(NoallocDevice* d, int vi, int* units) {
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (d->units[vi] > 0) { *units = d->units[vi]; return TG_OK; }
+    }
+    int u = 0;
+    cudaError_t e = kVariants[vi].units(&u);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (u <= 0) return fail(TG_ERR_UNSUPPORTED, "kernel variant %d cannot be resident on this device", vi);
+    std::lock_guard<std::mutex> lock(g_mu);
+    d->units[vi] = u;
+    *units = u;
+    return TG_OK;
+}
+
+// Host staging for one call's table: fixed per-thread storage, no heap.
+thread_local tg::Problem t_noalloc_host[TG_NOALLOC_MAX_PROBLEMS];
+
+}  // namespace
+
 // ========================================================================================
 // C ABI
 
@@ -442,6 +526,93 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
         e = cudaFreeAsync(ws, st);
         if (s != TG_OK) return s;
         if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(problem table)");
+    }
+    t_withhold = -1;
+    return TG_OK;
+}
+
+tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_stream_t stream) {
+    if (G < 0 || G > 65536) return fail(TG_ERR_INVALID_ARG, "G=%d out of range [0, 65536]", G);
+    if (G == 0) return TG_OK;
+    if (!table) return fail(TG_ERR_INVALID_ARG, "problem table is NULL");
+    int live = 0;
+    for (int g = 0; g < G; ++g) {
+        const tg_group_problem& t = table[g];
+        const Prob q{t.A, t.layout_a, t.lda, t.B, t.layout_b, t.ldb, t.C, t.c_dtype, t.ldc, t.M, t.N, t.K, t.epi, t.bias};
+        tg_status s = check(q, g);
+        if (s != TG_OK) return s;
+        live += (t.M > 0 && t.N > 0) ? 1 : 0;
+    }
+    if (live == 0) return TG_OK;
+    if (live > TG_NOALLOC_MAX_PROBLEMS)
+        return fail(TG_ERR_UNSUPPORTED,
+                    "%d non-empty problems, but the fixed no-alloc table holds at most %d; split the call or use "
+                    "tg_grouped_gemm", live, TG_NOALLOC_MAX_PROBLEMS);
+    NoallocDevice* d = nullptr;
+    tg_status s;
+    if ((s = noalloc_device(&d)) != TG_OK) return s;
+    if ((s = encoder()) != TG_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    // Classes (layout_a, layout_b, c_dtype) in order of first appearance; each
+    // class gets its own consecutive slice of the table and its own launch.
+    int class_order[8], n_classes = 0;
+    for (int g = 0; g < G; ++g) {
+        const tg_group_problem& t = table[g];
+        if (t.M == 0 || t.N == 0) continue;
+        const int key = (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) + (t.c_dtype == TG_F32 ? 1 : 0);
+        bool seen = false;
+        for (int c = 0; c < n_classes; ++c) seen = seen || class_order[c] == key;
+        if (!seen) class_order[n_classes++] = key;
+    }
+    const int64_t withhold = t_withhold;
+    int offset = 0;
+    for (int c = 0; c < n_classes; ++c) {
+        const int key = class_order[c];
+        const bool a_col = key & 4, b_col = key & 2, f32 = key & 1;
+        int64_t max_n = 0, rows = 0;
+        for (int g = 0; g < G; ++g) {
+            const tg_group_problem& t = table[g];
+            if (t.M == 0 || t.N == 0) continue;
+            const int k2 = (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) + (t.c_dtype == TG_F32 ? 1 : 0);
+            if (k2 != key) continue;
+            max_n = t.N > max_n ? t.N : max_n;
+            rows += t.M;
+        }
+        const TileChoice tc = pick_tile(rows, max_n, d->sms);
+        const int vi = variant_index(true, f32, tc.cta_group, tc.bn, a_col, !b_col);
+        const Variant& v = kVariants[vi];
+        int units = 0;
+        if ((s = noalloc_resident(d, vi, &units)) != TG_OK) return s;
+
+        tg::Problem* host = t_noalloc_host + offset;
+        int n = 0;
+        int64_t tiles = 0, max_tiles_n = 1;
+        for (int g = 0; g < G; ++g) {
+            const tg_group_problem& t = table[g];
+            if (t.M == 0 || t.N == 0) continue;
+            const int k2 = (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) + (t.c_dtype == TG_F32 ? 1 : 0);
+            if (k2 != key) continue;
+            const Prob q{t.A, t.layout_a, t.lda, t.B, t.layout_b, t.ldb, t.C, t.c_dtype, t.ldc, t.M, t.N, t.K, t.epi, t.bias};
+            if ((s = fill_problem(q, v, g, &host[n])) != TG_OK) return s;
+            host[n].tile_begin = tiles;
+            tiles += static_cast<int64_t>(host[n].tiles_m) * host[n].tiles_n;
+            if (host[n].tiles_n > max_tiles_n) max_tiles_n = host[n].tiles_n;
+            ++n;
+        }
+        cudaError_t e = cudaMemcpyAsync(d->table + offset, host, n * sizeof(tg::Problem), cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(no-alloc problem table)");
+        Params p;
+        std::memset(&p, 0, sizeof p);
+        p.problems = d->table + offset;
+        p.num_problems = n;
+        p.total_tiles = tiles;
+        p.band = pick_band(max_tiles_n, units);
+        p.err = d->err;
+        p.wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
+        p.withhold_kb = withhold;
+        if ((s = enqueue(p, v, units, st)) != TG_OK) return s;
+        offset += n;
     }
     t_withhold = -1;
     return TG_OK;

@@ -128,6 +128,35 @@ typedef struct tg_group_problem {
  */
 tg_status tg_grouped_gemm(const tg_group_problem *table, int G, tg_stream_t stream);
 
+/*
+ * Largest number of non-empty problems tg_grouped_gemm_noalloc accepts in one
+ * call: the size of its fixed device-side problem table.
+ */
+#define TG_NOALLOC_MAX_PROBLEMS 256
+
+/*
+ * tg_grouped_gemm_noalloc - tg_grouped_gemm for callers that may not allocate.
+ *
+ * The pages have no counterpart for this entry point; it exists for callers
+ * that must not allocate device memory once running (serving loops that
+ * reserve everything up front so a request can never stall or fail on an
+ * allocation, or programs whose device memory sits under another allocator's
+ * fixed budget).  It computes exactly what tg_grouped_gemm computes, with the
+ * same arguments, but calls no cudaMalloc, cudaFree or other allocating
+ * routine: the per-problem descriptors go into a fixed 128 KiB table compiled
+ * into the library (held on every GPU that loads libtg until process exit).
+ *
+ *   - At most TG_NOALLOC_MAX_PROBLEMS non-empty problems per call; more gives
+ *     TG_ERR_UNSUPPORTED (split the call, or use tg_grouped_gemm).
+ *   - The first call on each device looks up the table's device address
+ *     (cudaGetSymbolAddress) once; make that first call before any stream
+ *     capture on that device.
+ *   - Every call reuses the same table.  Calls ordered on one stream are safe;
+ *     calls that overlap on the GPU (different streams without ordering) race
+ *     and may compute with another call's descriptors.
+ */
+tg_status tg_grouped_gemm_noalloc(const tg_group_problem *table, int G, tg_stream_t stream);
+
 /* Static English description of a status code (never NULL). */
 const char *tg_status_string(tg_status status);
 
