@@ -23,7 +23,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -103,7 +102,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    """nvidia-smi clock / throttle-reason samples every 100 ms while running."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -118,7 +117,7 @@ class ClockSampler:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -238,12 +237,12 @@ class Part:
             r0, r1 = c.offsets[g], c.offsets[g + 1]
             rows = np.sort(rng.choice(r1 - r0, size=min(n_rows, r1 - r0), replace=False))
             oracle.gemm(wl.bf16_bits(c.a[r0:r1]), wl.bf16_bits(c.b[g]), rows=rows)
-            return 2 * len(rows) * c.N * c.K
+            return 2 * len(rows) * c.N * c.K, len(rows)
         rows = np.sort(rng.choice(c.M, size=min(n_rows, c.M), replace=False))
         bias = wl.bf16_bits(c.bias) if c.bias is not None else None
         oracle.gemm(wl.bf16_bits(c.a), wl.bf16_bits(c.b), a_col_major=c.a_col_major, b_col_major=c.b_col_major,
                     bias=bias, epi=c.epi, rows=rows)
-        return 2 * len(rows) * c.N * c.K
+        return 2 * len(rows) * c.N * c.K, len(rows)
 
 
 def oracle_sample(parts, target_s: float, seed: int = 0):
@@ -257,11 +256,11 @@ def oracle_sample(parts, target_s: float, seed: int = 0):
         n = 8
         while spent < share:
             t0 = time.perf_counter()
-            f = p.oracle_rows(n, seed + r_total)
+            f, done = p.oracle_rows(n, seed + r_total)
             dt = time.perf_counter() - t0
             flops += f
             spent += dt
-            r_total += n
+            r_total += done
             if spent < share:
                 n = int(min(max(n * 2, n * (share - spent) / max(dt, 1e-3)), 4096))
         secs += spent
@@ -358,20 +357,21 @@ def run_ours(args, parts_names):
         barrier(world)
         s0 = torch.cuda.Event(enable_timing=True)
         s1 = torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
         s0.record(stream)
         launches_e2e = 0
-        for _ in range(args.steps):
+        for _ in range(e2e_steps):
             for p in parts:
                 launches_e2e += p.e2e_step(stream)
         s1.record(stream)
         torch.cuda.synchronize()
         tg.device_status(stream)
-        e2e_ms = s0.elapsed_time(s1) / args.steps
+        e2e_ms = s0.elapsed_time(s1) / e2e_steps
         e2e_agg = aggregate(gather_max(e2e_ms, world), step_flops)
         e2e = {"value": e2e_agg["value_tflops"], "unit": "TFLOP/s",
                "h2d_bytes_per_step": sum(p.h2d_bytes for p in parts),
                "d2h_bytes_per_step": sum(p.d2h_bytes for p in parts),
-               "ms_per_step": e2e_agg["ms_per_step"], "gpu_launches": launches_e2e}
+               "ms_per_step": e2e_agg["ms_per_step"], "steps": e2e_steps, "gpu_launches": launches_e2e}
 
     if rank != 0:
         if world > 1:
@@ -426,8 +426,9 @@ def run_ours(args, parts_names):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=50, help="steps of the end-to-end loop (at most --steps)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--no-e2e", action="store_true")
