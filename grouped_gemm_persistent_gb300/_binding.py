@@ -67,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         lib.tg_gemm.restype = ci
         lib.tg_gemm.argtypes = [vp, ci, i64, vp, ci, i64, vp, ci, i64, i64, i64, i64, ci, vp, vp]
+        lib.tg_gemm_bcast.restype = ci
+        lib.tg_gemm_bcast.argtypes = [vp, ci, i64, i64, i64, vp, ci, i64, vp, ci, i64, i64, i64, ci, vp, vp]
         lib.tg_grouped_gemm.restype = ci
         lib.tg_grouped_gemm.argtypes = [ctypes.POINTER(GroupProblem), ci, vp]
         lib.tg_grouped_gemm_noalloc.restype = ci
@@ -151,6 +153,38 @@ def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, *, b
         raise ValueError("this epilogue needs a contiguous bf16 bias of length N")
     _check(load().tg_gemm(_ptr(a), la, lda, _ptr(b), lb, ldb, _ptr(out), F32 if out.dtype == torch.float32 else BF16,
                           ldc, M, N, K, epi, _ptr(bias) if epi else None, _stream_handle(stream)))
+    return out
+
+
+def gemm_bcast(a_user: torch.Tensor, b: torch.Tensor, repeat: int, out: torch.Tensor | None = None, *,
+               bias: torch.Tensor | None = None, epilogue: str = "none", out_dtype: torch.dtype = torch.bfloat16,
+               stream=None) -> torch.Tensor:
+    """out[U*repeat, N] = epilogue(A @ b) with A's row i*repeat + j equal to a_user[i] (tg_gemm_bcast).
+
+    The repeated rows are never materialised: the kernel reads ``a_user`` [U, K]
+    once per replica and stores each result row ``repeat`` times.
+    """
+    if a_user.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise TypeError("a_user and b must be torch.bfloat16")
+    U, K = a_user.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((U * repeat, N), dtype=out_dtype, device=a_user.device)
+    if tuple(out.shape) != (U * repeat, N):
+        raise ValueError("out must be [U * repeat, N]")
+    la, lda = _matrix(a_user, "a_user")
+    lb, ldb = _matrix(b, "b")
+    lc, ldc = _matrix(out, "out")
+    if lc != ROW_MAJOR:
+        raise ValueError("out must be row-major")
+    epi = EPILOGUES[epilogue]
+    if epi and (bias is None or bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("this epilogue needs a contiguous bf16 bias of length N")
+    _check(load().tg_gemm_bcast(_ptr(a_user), la, lda, U, repeat, _ptr(b), lb, ldb, _ptr(out),
+                                F32 if out.dtype == torch.float32 else BF16, ldc, N, K, epi,
+                                _ptr(bias) if epi else None, _stream_handle(stream)))
     return out
 
 

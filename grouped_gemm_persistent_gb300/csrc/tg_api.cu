@@ -149,6 +149,22 @@ tg_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint
     return TG_OK;
 }
 
+// 3-D map [outer][mid][inner] with strides (in bytes) for the two outer dimensions.
+tg_status make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t mid,
+                      uint64_t outer, uint64_t mid_stride, uint64_t outer_stride, uint32_t box_inner,
+                      uint32_t box_mid, uint32_t box_outer, const char* what) {
+    const cuuint64_t dims[3] = {inner, mid, outer};
+    const cuuint64_t strides[2] = {mid_stride, outer_stride};
+    const cuuint32_t box[3] = {box_inner, box_mid, box_outer};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, int(r));
+    return TG_OK;
+}
+
 // ----------------------------------------------------------------------------------------
 // argument checks
 
@@ -313,6 +329,9 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     out->tiles_m = static_cast<int32_t>((q.M + v.tile_m - 1) / v.tile_m);
     out->tiles_n = static_cast<int32_t>((q.N + v.bn - 1) / v.bn);
     out->k_blocks = static_cast<int32_t>((q.K + tg::BK - 1) / tg::BK);
+    out->repeat = 0;
+    out->replicas = 1;
+    out->split_begin = INT32_MAX;
     return TG_OK;
 }
 
@@ -447,6 +466,67 @@ tg_status tg_gemm(const void* A, tg_layout layout_a, int64_t lda, const void* B,
     p.problems = nullptr;
     p.num_problems = 1;
     p.total_tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
+    p.band = pick_band(p.dense.tiles_n, units);
+    // A last wave at most half full is split into half-width tiles, so it takes
+    // half a tile time (TG_SPLIT_TAIL=0 turns this off).
+    const int64_t rem = p.total_tiles % units;
+    const char* split_env = std::getenv("TG_SPLIT_TAIL");
+    const bool split_ok = !(split_env && split_env[0] == '0') && v.bn == 256 && v.bn_cta / 2 % 64 == 0;
+    if (split_ok && rem > 0 && 2 * rem <= units && K > 0) {
+        p.dense.split_begin = static_cast<int32_t>(p.total_tiles - rem);
+        p.total_tiles += rem;
+        if (layout_b == TG_COL_MAJOR) {
+            if ((s = make_map(&p.dense_b_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, ldb * 2, 64, v.bn_cta / 2,
+                              "B (half-width tiles)", 0)) != TG_OK)
+                return s;
+        }
+    }
+    base_params(&p, d);
+    return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int64_t U, int64_t repeat,
+                        const void* B, tg_layout layout_b, int64_t ldb, void* C, tg_dtype c_dtype, int64_t ldc,
+                        int64_t N, int64_t K, tg_epilogue epi, const void* bias, tg_stream_t stream) {
+    if (repeat < 1) return fail(TG_ERR_INVALID_ARG, "repeat=%lld must be at least 1", (long long)repeat);
+    if (U < 0) return fail(TG_ERR_INVALID_ARG, "negative U=%lld", (long long)U);
+    if (U > 0 && repeat > kMaxDim / U)
+        return fail(TG_ERR_UNSUPPORTED, "U * repeat must be below 2^31 (U=%lld, repeat=%lld)", (long long)U,
+                    (long long)repeat);
+    const Prob q{A_user, layout_a, lda, B, layout_b, ldb, C, c_dtype, ldc, U, N, K, epi, bias};
+    tg_status s = check(q, 0);
+    if (s != TG_OK) return s;
+    if (U == 0 || N == 0) return TG_OK;
+    DeviceState* d = nullptr;
+    if ((s = device_state(&d)) != TG_OK) return s;
+    if ((s = encoder()) != TG_OK) return s;
+
+    // Single-CTA tiles over the user rows; the broadcast store is what costs, so
+    // each tile is recomputed by `replicas` CTAs that split its repeat indices.
+    TileChoice tc = pick_tile(U, N, d->sms);
+    tc.cta_group = 1;
+    const int vi = variant_index(false, c_dtype == TG_F32, 1, tc.bn, layout_a == TG_COL_MAJOR, layout_b == TG_ROW_MAJOR);
+    const Variant& v = kVariants[vi];
+    int units = 0;
+    if ((s = resident(d, vi, &units)) != TG_OK) return s;
+
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    if ((s = fill_problem(q, v, 0, &p.dense)) != TG_OK) return s;
+    const bool f32 = c_dtype == TG_F32;
+    const uint64_t row = static_cast<uint64_t>(ldc) * (f32 ? 4 : 2);
+    if ((s = make_map_3d(&p.dense.tma_c, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C,
+                         N, repeat, U, row, row * repeat, v.cw, 1, 32, "C (broadcast view)")) != TG_OK)
+        return s;
+    const int64_t tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
+    int64_t replicas = units / tiles;
+    if (replicas < 1) replicas = 1;
+    if (replicas > repeat) replicas = repeat;
+    p.dense.repeat = static_cast<int32_t>(repeat);
+    p.dense.replicas = static_cast<int32_t>(replicas);
+    p.dense.tile_begin = 0;
+    p.num_problems = 1;
+    p.total_tiles = tiles * replicas;
     p.band = pick_band(p.dense.tiles_n, units);
     base_params(&p, d);
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));

@@ -74,11 +74,23 @@ struct alignas(128) Problem {
     int32_t M, N, K;
     int32_t epi;
     int32_t tiles_m, tiles_n, k_blocks;
-    int32_t reserved;
+    // Broadcast form (repeat > 0): rows of A are U distinct "user" rows and
+    // output row i * repeat + j (j < repeat) is user row i's result; tma_c is a
+    // 3-D view [U][repeat][N] of C.  Each (M-tile, N-tile) is computed by
+    // `replicas` CTAs, replica r storing the repeat indices
+    // [r * repeat / replicas, (r + 1) * repeat / replicas).
+    int32_t repeat;
+    int32_t replicas;           // >= 1
+    // Local tile indices >= split_begin are half-width tiles (BN/2 columns): the
+    // last, partly filled wave of a dense launch is split in two along N so it
+    // takes half a tile time.  Half tile u covers full tile split_begin + u/2,
+    // columns [BN/2 * (u % 2), BN/2 * (u % 2 + 1)).  INT32_MAX: no split.
+    int32_t split_begin;
 };
 
 struct Params {
     Problem dense;              // the problem of a dense launch (lives in parameter space)
+    CUtensorMap dense_b_half;   // B map with a BN_CTA/2-row box, for half-width tiles of column-major B
     const Problem* problems;    // grouped launch: device array written by the host
     int32_t num_problems;
     int32_t band;               // raster band width in N-tiles
@@ -121,6 +133,8 @@ struct Config {
     static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 
     static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TILE_M, BN, A_MN, B_MN);
+    static constexpr uint32_t IDESC_HALF = ptx::idesc_bf16_f32(TILE_M, BN / 2, A_MN, B_MN);
+    static constexpr bool CAN_SPLIT = (BN_CTA / 2) % 64 == 0;   // half-width B still in whole 64-column boxes
 
     static_assert(BN == 128 || BN == 256, "tile width");
     static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "cta group");
@@ -138,6 +152,8 @@ struct TileCoord {
     int g;        // problem index
     int m0;       // first accumulator row of this CTA
     int n0;       // first column of the tile
+    int r;        // replica index (broadcast form), else 0
+    int width;    // tile columns: BN, or BN/2 for a split tail tile
 };
 
 template <class Cfg>
@@ -160,7 +176,18 @@ __device__ __forceinline__ int find_problem(const Params& p, int64_t t, int g) {
 template <class Cfg>
 __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int g, uint32_t rank) {
     const Problem& pr = problem_of<Cfg>(p, g);
-    const int64_t local = t - pr.tile_begin;
+    int64_t local = t - pr.tile_begin;
+    int replica = 0;
+    if (pr.replicas > 1) {   // replicas of one tile are adjacent: they share A and B in L2
+        replica = static_cast<int>(local % pr.replicas);
+        local /= pr.replicas;
+    }
+    int half = -1;
+    if (local >= pr.split_begin) {
+        const int64_t u = local - pr.split_begin;
+        local = pr.split_begin + u / 2;
+        half = static_cast<int>(u & 1);
+    }
     const int band = p.band;
     const int64_t per_band = static_cast<int64_t>(pr.tiles_m) * band;
     const int b = static_cast<int>(local / per_band);
@@ -173,6 +200,12 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     c.g = g;
     c.m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
     c.n0 = nb * Cfg::BN;
+    c.r = replica;
+    c.width = Cfg::BN;
+    if (half >= 0) {
+        c.width = Cfg::BN / 2;
+        c.n0 += half * (Cfg::BN / 2);
+    }
     return c;
 }
 
@@ -342,7 +375,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     }
                 }
                 const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
-                const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;
+                const bool full_width = tc.width == Cfg::BN;
+                const int b_cols = full_width ? Cfg::BN_CTA : Cfg::BN_CTA / 2;    // B columns this CTA loads
+                const int nb0 = tc.n0 + static_cast<int>(rank) * b_cols;
+                const uint32_t stage_bytes = Cfg::A_BYTES + (full_width ? Cfg::B_BYTES : Cfg::B_BYTES / 2);
+                const CUtensorMap* b_map = &pr.tma_b;
+                if constexpr (!Cfg::GROUPED && !Cfg::B_MN) {
+                    if (!full_width) b_map = &p.dense_b_half;
+                }
                 for (int kb = 0; kb < pr.k_blocks; ++kb) {
                     if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, t, stage)) {
                         aborted = true;
@@ -351,7 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     const bool skip = withhold && kb == p.withhold_kb;
                     if (!skip) {
                         const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
-                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES * CG);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes * CG);
                         const int k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * Cfg::A_BYTES;
                         const uint32_t b_dst = sB + stage * Cfg::B_BYTES;
@@ -366,10 +406,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             load(a_dst, &pr.tma_a, k0, tc.m0);
                         }
                         if constexpr (Cfg::B_MN) {
-#pragma unroll
-                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+                            for (int j = 0; j < b_cols / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
                         } else {
-                            load(b_dst, &pr.tma_b, k0, nb0);
+                            load(b_dst, b_map, k0, nb0);
                         }
                         ++issued;
                     }
@@ -407,6 +446,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             for (int64_t t = unit; t < p.total_tiles && !aborted; t += num_units) {
                 g = find_problem<Cfg>(p, t, g);
                 const Problem& pr = problem_of<Cfg>(p, g);
+                const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
+                const uint32_t idesc = tc.width == Cfg::BN ? Cfg::IDESC : Cfg::IDESC_HALF;
                 if (!wait_bounded<CG>(tempty_bar(acc), acc_phase ^ 1u, p, abort_addr, ROLE_MMA, t, 16 + acc)) {
                     aborted = true;
                     break;
@@ -431,7 +472,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         // swizzled row; MN-major: 16 rows (2048 bytes) further down.
                         const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
                         const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
-                        ptx::mma_bf16<CG>(d_tmem, a_desc + a_off, b_desc + b_off, Cfg::IDESC,
+                        ptx::mma_bf16<CG>(d_tmem, a_desc + a_off, b_desc + b_off, idesc,
                                           (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     any_mma = true;
@@ -498,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             __syncwarp();
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
-            constexpr int CHUNKS = BN / Cfg::CW;
+            const int CHUNKS = tc.width / Cfg::CW;
 #pragma unroll 1
             for (int c = 0; c < CHUNKS; ++c) {
                 float v[Cfg::CW];
@@ -563,7 +604,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::tma_store_2d(&pr.tma_c, buf, n_chunk, row0);
+                    if (pr.repeat > 0) {
+                        // broadcast: the same 32 user rows go to every repeat index of this replica
+                        const int j0 = static_cast<int>(static_cast<int64_t>(tc.r) * pr.repeat / pr.replicas);
+                        const int j1 = static_cast<int>(static_cast<int64_t>(tc.r + 1) * pr.repeat / pr.replicas);
+                        for (int j = j0; j < j1; ++j) ptx::tma_store_3d(&pr.tma_c, buf, n_chunk, j, row0);
+                    } else {
+                        ptx::tma_store_2d(&pr.tma_c, buf, n_chunk, row0);
+                    }
                     ptx::bulk_commit_group();
                 }
                 sbuf ^= 1;

@@ -127,6 +127,12 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
                  :: "l"(tmap), "r"(x), "r"(y), "r"(src) : "memory");
 }
 
+// 3-D tiled store own shared memory -> global (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 :: "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(src) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

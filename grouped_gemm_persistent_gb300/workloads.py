@@ -61,10 +61,19 @@ class DenseCase:
     epi: str                   # "none", "bias", "bias_gelu"
     seed: int
     recipe: str = ""
+    users: torch.Tensor | None = None   # broadcast form: the distinct A rows (A[i] = users[i // repeat])
+    repeat: int = 1
 
     @property
     def flops(self) -> int:
         return 2 * self.M * self.N * self.K
+
+    @property
+    def bcast_bytes(self) -> int:
+        """Algorithmic bytes of the broadcast form: user rows, B, bias read once, C written once."""
+        cb = 2 if self.c_dtype == "bf16" else 4
+        nb = 2 * self.N if self.bias is not None else 0
+        return 2 * self.users.shape[0] * self.K + 2 * self.K * self.N + cb * self.M * self.N + nb
 
     @property
     def algorithmic_bytes(self) -> int:
@@ -163,7 +172,8 @@ def skinny_bcast(M: int = 131072, K: int = 1024, N: int = 128, repeat: int = 128
     b = _draw(gen, (K, N), "normal", 1.0 / math.sqrt(K))
     bias = (torch.randn((N,), generator=gen, dtype=torch.float32) * 0.1).to(torch.bfloat16)
     return DenseCase("skinny_bcast", M, N, K, a, b, bias, False, False, "bf16", "bias", seed,
-                     recipe=f"{M // repeat} user rows N(0,1) x{repeat}, B N(0,1)/sqrt(K), seed {seed}")
+                     recipe=f"{M // repeat} user rows N(0,1) x{repeat}, B N(0,1)/sqrt(K), seed {seed}",
+                     users=users, repeat=repeat)
 
 
 def moe_counts(G: int, tokens: int, alpha: float, seed: int) -> np.ndarray:

@@ -97,6 +97,30 @@ tg_status tg_gemm(const void *A, tg_layout layout_a, int64_t lda,
                   tg_stream_t stream);
 
 /*
+ * tg_gemm_bcast - dense GEMM whose A rows are repeated: in-kernel broadcast.
+ *
+ * C[U * repeat, N] = epilogue(A . B) where row i * repeat + j of A (j < repeat)
+ * is row i of A_user[U, K]: each user's `repeat` candidate rows are contiguous
+ * in C.  This is the in-kernel broadcast of the TLX article's second case study
+ * ("In-kernel broadcast optimization for RecSys"): instead of materialising the
+ * repeated user rows, the kernel consumes A_user at its own batch size and
+ * broadcasts inside the kernel.  Each distinct result row is computed once per
+ * replica CTA and stored `repeat` times, so A costs U*K*2 bytes of traffic
+ * instead of U*repeat*K*2.  Results are bitwise identical to tg_gemm on the
+ * materialised A.
+ *
+ *   A_user, layout_a, lda : bf16 U x K (row-major: lda >= K; column-major: lda >= U).
+ *   repeat                : >= 1; U * repeat < 2^31.
+ *   other arguments       : as tg_gemm, with M = U * repeat rows of C (ldc >= N).
+ */
+tg_status tg_gemm_bcast(const void *A_user, tg_layout layout_a, int64_t lda, int64_t U, int64_t repeat,
+                        const void *B, tg_layout layout_b, int64_t ldb,
+                        void *C, tg_dtype c_dtype, int64_t ldc,
+                        int64_t N, int64_t K,
+                        tg_epilogue epi, const void *bias,
+                        tg_stream_t stream);
+
+/*
  * One problem of a grouped GEMM: C_g = epilogue_g(A_g . B_g), fields as in
  * tg_gemm.  Problems are independent and may differ in every field; a problem
  * with M == 0 or N == 0 (an expert that received no tokens) is skipped and its

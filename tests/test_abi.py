@@ -138,3 +138,14 @@ def test_valid_call_without_device_fails_loudly():
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
     rc = int(out.stdout.strip().splitlines()[-1])
     assert rc in (tg.TG_ERR_NO_DEVICE, tg.TG_ERR_CUDA)
+
+
+def test_bcast_argument_checks(lib):
+    def bc(U=64, repeat=4, A=ALIGNED, lda=64, C=ALIGNED_C, K=64, N=64):
+        return lib.tg_gemm_bcast(A, 0, lda, U, repeat, ALIGNED_B, 0, 64, C, 0, 64, N, K, 0, None, None)
+    assert bc(repeat=0) == tg.TG_ERR_INVALID_ARG
+    assert bc(U=-1) == tg.TG_ERR_INVALID_ARG
+    assert bc(U=1 << 20, repeat=1 << 12) == tg.TG_ERR_UNSUPPORTED      # U * repeat >= 2^31
+    assert bc(C=None) == tg.TG_ERR_INVALID_ARG
+    assert bc(lda=32) == tg.TG_ERR_INVALID_ARG
+    assert bc(U=0) == tg.TG_OK

@@ -39,6 +39,13 @@ def tile(request, monkeypatch):
     return request.param
 
 
+@pytest.fixture(params=["split", "nosplit"])
+def split(request, monkeypatch):
+    """Dense launches split a partly filled last wave into half-width tiles unless TG_SPLIT_TAIL=0."""
+    monkeypatch.setenv("TG_SPLIT_TAIL", "1" if request.param == "split" else "0")
+    return request.param
+
+
 @pytest.fixture(autouse=True, scope="module")
 def _built():
     from grouped_gemm_persistent_gb300.build import build
@@ -62,7 +69,7 @@ def test_dense_256_workload():
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("epi", ["none", "bias", "bias_gelu"])
 @pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
-def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype, tile):
+def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype, tile, split):
     # spans several tiles with a ragged tail in M, N and K (K not a multiple of 64)
     case = wl.dense_random(333, 392, 200, seed=100, dist="uniform", a_col_major=a_col, b_col_major=b_col,
                            epi=epi, c_dtype=c_dtype, **lds(333, 392, 200, a_col, b_col))
@@ -92,7 +99,7 @@ def test_padded_leading_dimensions():
     assert torch.isnan(c_full[:, 136:].float()).all(), "columns beyond N were written"
 
 
-def test_integer_exact_bitwise(tile):
+def test_integer_exact_bitwise(tile, split):
     # integers in [-4, 4]: every fp32 partial sum is exact, so C must equal the
     # exact result bit for bit (fp32 out) and its RNE rounding (bf16 out)
     for a_col, b_col in LAYOUTS:
@@ -148,7 +155,7 @@ def test_empty_m_or_n_writes_nothing():
     _sync_ok()
 
 
-def test_guard_bands_untouched(tile):
+def test_guard_bands_untouched(tile, split):
     case = wl.dense_random(300, 264, 128, seed=12, dist="normal", epi="bias")
     big = torch.full((300 + 64, 264 + 40), float("inf"), dtype=torch.float32, device="cuda")
     out = big[32:332, 8:272]
@@ -187,6 +194,40 @@ def test_side_stream():
     with torch.cuda.stream(s):
         c = tg.gemm(a, b, stream=s)
     tg.device_status(s)
+    check_dense(case, c)
+
+
+# ------------------------------------------------------------------------------------------ in-kernel broadcast
+
+@pytest.mark.parametrize("U,repeat,N,K", [(37, 5, 136, 72), (300, 1, 264, 128), (5, 300, 128, 64),
+                                          (129, 3, 392, 200), (256, 40, 128, 1024)])
+@pytest.mark.parametrize("epi", ["none", "bias", "bias_gelu"])
+def test_bcast_matches_materialised(U, repeat, N, K, epi):
+    gen = torch.Generator().manual_seed(U + repeat + N + K)
+    users = (torch.randn((U, K), generator=gen) / 4).to(torch.bfloat16)
+    b = (torch.randn((K, N), generator=gen) / 4).to(torch.bfloat16)
+    bias = (torch.randn(N, generator=gen) * 0.1).to(torch.bfloat16)
+    out = torch.full((U * repeat, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tg.gemm_bcast(users.cuda(), b.cuda(), repeat, out, bias=bias.cuda(), epilogue=epi)
+    _sync_ok()
+    a = users.repeat_interleave(repeat, dim=0)          # the materialised A the definition refers to
+    y, s = oracle.gemm(wl.bf16_bits(a), wl.bf16_bits(b), bias=wl.bf16_bits(bias), epi=epi)
+    r = oracle.compare(to_f64(out), y, s, np.abs(bias.double().numpy()) if epi != "none" else None)
+    assert r["ok"] and r["max_tight"] < 4.0, r
+
+
+def test_bcast_equals_dense_on_materialised_bitwise():
+    case = wl.dense_case("skinny_bcast")
+    dense = run_dense(case)
+    bc = tg.gemm_bcast(case.users.cuda(), case.b.cuda(), case.repeat, bias=case.bias.cuda(), epilogue="bias")
+    _sync_ok()
+    assert torch.equal(dense.view(torch.int16), bc.view(torch.int16))
+
+
+def test_workload_skinny_bcast_in_kernel_broadcast_full():
+    case = wl.dense_case("skinny_bcast")
+    c = tg.gemm_bcast(case.users.cuda(), case.b.cuda(), case.repeat, bias=case.bias.cuda(), epilogue="bias")
+    _sync_ok()
     check_dense(case, c)
 
 
