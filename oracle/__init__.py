@@ -55,7 +55,9 @@ class Oracle:
         vp = ctypes.c_void_p
         lib.oracle_gemm.restype = ctypes.c_int
         lib.oracle_gemm.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64,
-                                    vp, ctypes.c_int, i64, i64, i64, vp, i64, dp, dp]
+                                    vp, ctypes.c_int, ctypes.c_int, i64, i64, i64, vp, i64, dp, dp]
+        lib.oracle_f16_to_double.restype = ctypes.c_double
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_double.restype = ctypes.c_double
         lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_gelu_tanh.restype = ctypes.c_double
@@ -64,8 +66,9 @@ class Oracle:
         self.lib = lib
         self.path = path
 
-    def gemm(self, a, b, *, a_col_major=False, b_col_major=False, bias=None, epi="none", rows=None):
-        return _gemm(self.lib, a, b, a_col_major, b_col_major, bias, epi, rows)
+    def gemm(self, a, b, *, a_col_major=False, b_col_major=False, bias=None, epi="none", rows=None,
+             in_dtype="bf16"):
+        return _gemm(self.lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype)
 
     def gelu_tanh(self, z: float) -> float:
         return self.lib.oracle_gelu_tanh(z)
@@ -88,6 +91,10 @@ def bf16_to_double(bits: int) -> float:
     return default().lib.oracle_bf16_to_double(bits)
 
 
+def f16_to_double(bits: int) -> float:
+    return default().lib.oracle_f16_to_double(bits)
+
+
 def gelu_tanh(z: float) -> float:
     return default().gelu_tanh(z)
 
@@ -104,20 +111,24 @@ def _storage(x: np.ndarray, name: str):
 
 
 def gemm(a: np.ndarray, b: np.ndarray, *, a_col_major: bool = False, b_col_major: bool = False,
-         bias: np.ndarray | None = None, epi: str = "none", rows=None):
+         bias: np.ndarray | None = None, epi: str = "none", rows=None, in_dtype: str = "bf16"):
     """Reference y and s for C = epi(A . B).
 
     ``a`` is A's storage: [M, K] (row-major) or [K, M] (column-major, i.e.
     A^T stored row-major).  ``b`` is [K, N] (row-major) or [N, K]
     (column-major).  Both hold bf16 bit patterns as uint16; a row stride
     larger than the row (a padded leading dimension) is allowed.  ``bias`` is
-    uint16 [N].  ``rows`` selects output rows (default: all).
+    uint16 [N].  ``rows`` selects output rows (default: all).  ``in_dtype``
+    ("bf16" or "f16") is the element type the bit patterns of a, b and bias hold.
     Returns (y, s), float64 arrays [len(rows), N].
     """
-    return _gemm(default().lib, a, b, a_col_major, b_col_major, bias, epi, rows)
+    return _gemm(default().lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype)
 
 
-def _gemm(lib, a, b, a_col_major, b_col_major, bias, epi, rows):
+IN_DTYPES = {"bf16": 0, "f16": 1}
+
+
+def _gemm(lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype="bf16"):
     pa, lda = _storage(a, "a")
     pb, ldb = _storage(b, "b")
     M, K = (a.shape[1], a.shape[0]) if a_col_major else a.shape
@@ -138,7 +149,7 @@ def _gemm(lib, a, b, a_col_major, b_col_major, bias, epi, rows):
         prow, nrow = keep.ctypes.data, keep.shape[0]
     y = np.empty((nrow, N), dtype=np.float64)
     s = np.empty((nrow, N), dtype=np.float64)
-    rc = lib.oracle_gemm(pa, int(a_col_major), lda, pb, int(b_col_major), ldb, pbias, e,
+    rc = lib.oracle_gemm(pa, int(a_col_major), lda, pb, int(b_col_major), ldb, pbias, e, IN_DTYPES[in_dtype],
                          M, N, K, prow, nrow,
                          y.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                          s.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
@@ -162,7 +173,7 @@ def grouped_gemm(problems, rows_per_group=None):
         rows = None if rows_per_group is None else rows_per_group[g]
         out.append(gemm(p["a"], p["b"], a_col_major=p.get("a_col_major", False),
                         b_col_major=p.get("b_col_major", False), bias=p.get("bias"),
-                        epi=p.get("epi", "none"), rows=rows))
+                        epi=p.get("epi", "none"), rows=rows, in_dtype=p.get("in_dtype", "bf16")))
     return out
 
 

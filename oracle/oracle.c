@@ -1,5 +1,5 @@
 /*
- * oracle.c - plain CPU reference for C = epilogue(A . B) on bf16 inputs.
+ * oracle.c - plain CPU reference for C = epilogue(A . B) on bf16 or fp16 inputs.
  *
  * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only
  * the test suite, the package's smoke check and the benchmark's CPU-baseline
@@ -17,9 +17,10 @@
  *          = gelu_tanh(x_ij + bias_j)         epilogue "bias + GELU"
  *
  * The listing accumulates in fp32 over BLOCK_K steps; the oracle is the
- * plain definition that result approximates: every bf16 input is widened
+ * plain definition that result approximates: every input is widened
  * exactly to double, every product a_ik*b_kj is exact in double (8+8
- * significand bits), and the sum runs over k in ascending order in double.
+ * significand bits for bf16, 11+11 for fp16), and the sum runs over k in
+ * ascending order in double.
  * No blocking, no reordering: one output element is one dot product.
  *
  * Beside y it returns s_ij = sum_k |a_ik * b_kj|, the magnitude that the
@@ -30,9 +31,12 @@
  * (Hendrycks & Gimpel, "Gaussian Error Linear Units"), in double with the C
  * library's tanh.
  *
+ * Element types: A, B and bias are all bf16 or all IEEE binary16 (fp16, the
+ * TLX listing's type); both widen exactly to double.
+ *
  * Layouts: A is M x K, row-major (element (i,k) at A[i*lda + k]) or
  * column-major (at A[k*lda + i]); B is K x N, row-major (B[k*ldb + j]) or
- * column-major (B[j*ldb + k]).  Inputs are bf16 bit patterns (uint16).
+ * column-major (B[j*ldb + k]).  Inputs are bit patterns (uint16).
  *
  * Rows: the caller may ask for a subset of output rows (rows != NULL), so a
  * full-size problem can be checked on a sample; row r of Y/S then holds
@@ -58,6 +62,31 @@ double oracle_bf16_to_double(uint16_t h)
     return (double)f;
 }
 
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Normal: (-1)^s * 2^(e-15) * (1 + f/1024); subnormal (e = 0): (-1)^s * 2^-14 * f/1024;
+ * e = 31: infinity (f = 0) or NaN.  Every value is exact in double. */
+double oracle_f16_to_double(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1f;
+    const int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+enum { ORACLE_IN_BF16 = 0, ORACLE_IN_F16 = 1 };
+
+static double widen(uint16_t h, int in_dtype)
+{
+    return in_dtype == ORACLE_IN_F16 ? oracle_f16_to_double(h) : oracle_bf16_to_double(h);
+}
+
 double oracle_gelu_tanh(double z)
 {
     const double c = sqrt(2.0 / 3.14159265358979323846);
@@ -79,12 +108,13 @@ int oracle_num_threads(void)
  */
 int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
                 const uint16_t *B, int b_col_major, int64_t ldb,
-                const uint16_t *bias, int epi,
+                const uint16_t *bias, int epi, int in_dtype,
                 int64_t M, int64_t N, int64_t K,
                 const int64_t *rows, int64_t n_rows,
                 double *Y, double *S)
 {
     if (M < 0 || N < 0 || K < 0 || !Y || !S) return -1;
+    if (in_dtype != ORACLE_IN_BF16 && in_dtype != ORACLE_IN_F16) return -1;
     if (epi != ORACLE_EPI_NONE && epi != ORACLE_EPI_BIAS && epi != ORACLE_EPI_BIAS_GELU) return -1;
     if (epi != ORACLE_EPI_NONE && N > 0 && !bias) return -1;
     if (K > 0 && M > 0 && !A) return -1;
@@ -101,7 +131,7 @@ int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
         if (!b) return -2;
         for (int64_t k = 0; k < K; ++k)
             for (int64_t j = 0; j < N; ++j)
-                b[k * N + j] = oracle_bf16_to_double(b_col_major ? B[j * ldb + k] : B[k * ldb + j]);
+                b[k * N + j] = widen(b_col_major ? B[j * ldb + k] : B[k * ldb + j], in_dtype);
     }
 
 #pragma omp parallel for schedule(dynamic, 1)
@@ -113,7 +143,7 @@ int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
         /* k ascending, the same order for every element: y_ij accumulates
          * a_ik*b_kj for k = 0, 1, ..., K-1. */
         for (int64_t k = 0; k < K; ++k) {
-            const double a = oracle_bf16_to_double(a_col_major ? A[k * lda + i] : A[i * lda + k]);
+            const double a = widen(a_col_major ? A[k * lda + i] : A[i * lda + k], in_dtype);
             const double *bk = b + k * N;
             for (int64_t j = 0; j < N; ++j) {
                 const double p = a * bk[j];
@@ -123,7 +153,7 @@ int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
         }
         if (epi != ORACLE_EPI_NONE) {
             for (int64_t j = 0; j < N; ++j) {
-                const double z = y[j] + oracle_bf16_to_double(bias[j]);
+                const double z = y[j] + widen(bias[j], in_dtype);
                 y[j] = (epi == ORACLE_EPI_BIAS_GELU) ? oracle_gelu_tanh(z) : z;
             }
         }

@@ -193,8 +193,36 @@ def pin_rows_and_degenerate(orc):
     assert ye.shape == (0, 33)
 
 
+def pin_f16_widening_exhaustive(orc):
+    # every binary16 bit pattern against numpy's float16 -> float64 conversion
+    allbits = np.arange(65536, dtype=np.uint16)
+    ref = allbits.view(np.float16).astype(np.float64)
+    ours = np.array([orc.lib.oracle_f16_to_double(int(h)) for h in allbits])
+    same = (ours == ref) | (np.isnan(ours) & np.isnan(ref))
+    assert same.all(), f"f16 widening differs at {np.flatnonzero(~same)[:8]}"
+    assert np.array_equal(np.signbit(ours[~np.isnan(ours)]), np.signbit(ref[~np.isnan(ref)]))
+
+
+def pin_f16_gemm(orc):
+    # fp16 operands: integer-exact product against int64 matmul, and a random one against torch float64
+    rng = np.random.default_rng(17)
+    A = rng.integers(-8, 9, (23, 70))
+    B = rng.integers(-8, 9, (70, 19))
+    bias = rng.integers(-4, 5, 19)
+    f16 = lambda x: np.asarray(x, dtype=np.float16).view(np.uint16)
+    y, S = orc.gemm(f16(A), f16(B), bias=f16(bias), epi="bias", in_dtype="f16")
+    assert np.array_equal(y, (A @ B + bias[None, :]).astype(np.float64))
+    assert np.array_equal(S, (np.abs(A) @ np.abs(B)).astype(np.float64))
+    a = rng.standard_normal((31, 45)).astype(np.float16)
+    b = rng.standard_normal((45, 27)).astype(np.float16)
+    y, S = orc.gemm(a.view(np.uint16), np.ascontiguousarray(b.T).view(np.uint16), b_col_major=True, in_dtype="f16")
+    ref = a.astype(np.float64) @ b.astype(np.float64)
+    assert np.all(np.abs(y - ref) <= 1e-12 * S)
+
+
 PINS = [pin_golden, pin_identity_permutation, pin_rank1, pin_integer_exact,
-        pin_fraction_bruteforce, pin_torch_float64, pin_gelu, pin_rows_and_degenerate]
+        pin_fraction_bruteforce, pin_torch_float64, pin_gelu, pin_rows_and_degenerate,
+        pin_f16_widening_exhaustive, pin_f16_gemm]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -221,13 +249,15 @@ def test_compare_detects_errors():
 
 MUTANTS = {
     "dropped_last_k": ("for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 0; k + 1 < K; ++k) {"),
-    "transposed_b": ("B[k * ldb + j]);", "B[j * ldb + k]);"),
-    "bias_sign": ("y[j] + oracle_bf16_to_double(bias[j])", "y[j] - oracle_bf16_to_double(bias[j])"),
-    "bias_index": ("oracle_bf16_to_double(bias[j])", "oracle_bf16_to_double(bias[0])"),
+    "transposed_b": ("B[k * ldb + j], in_dtype);", "B[j * ldb + k], in_dtype);"),
+    "bias_sign": ("y[j] + widen(bias[j], in_dtype)", "y[j] - widen(bias[j], in_dtype)"),
+    "bias_index": ("widen(bias[j], in_dtype)", "widen(bias[0], in_dtype)"),
     "gelu_cubic": ("0.044715 * z * z * z", "0.044715 * z * z"),
     "gelu_scale": ("sqrt(2.0 / 3.14159265358979323846)", "sqrt(1.0 / 3.14159265358979323846)"),
     "s_not_abs": ("s[j] += fabs(p);", "s[j] += p;"),
-    "a_k_reversed": ("A[i * lda + k]);", "A[i * lda + (K - 1 - k)]);"),
+    "a_k_reversed": ("A[i * lda + k], in_dtype);", "A[i * lda + (K - 1 - k)], in_dtype);"),
+    "f16_exponent_bias": ("v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);"),
+    "f16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
 }
 
 
