@@ -15,7 +15,8 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtg.so")
+# TG_LIB_PATH selects another build of the library (e.g. to compare two builds on one GPU).
+LIB_PATH = os.environ.get("TG_LIB_PATH") or os.path.join(_PKG, "libtg.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "tg.h")
 
 TG_OK, TG_ERR_INVALID_ARG, TG_ERR_UNSUPPORTED, TG_ERR_CUDA, TG_ERR_TIMEOUT, TG_ERR_NO_DEVICE = range(6)
@@ -23,7 +24,8 @@ STATUS_NAMES = {0: "TG_OK", 1: "TG_ERR_INVALID_ARG", 2: "TG_ERR_UNSUPPORTED", 3:
                 4: "TG_ERR_TIMEOUT", 5: "TG_ERR_NO_DEVICE"}
 EPILOGUES = {"none": 0, "bias": 1, "bias_gelu": 2}
 ROW_MAJOR, COL_MAJOR = 0, 1
-BF16, F32 = 0, 1
+BF16, F32, F16 = 0, 1, 2
+_DTYPE_CODE = {torch.bfloat16: BF16, torch.float32: F32, torch.float16: F16}
 
 _lib = None
 _lock = threading.Lock()
@@ -44,6 +46,7 @@ class GroupProblem(ctypes.Structure):
         ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64), ("c_dtype", ctypes.c_int),
         ("epi", ctypes.c_int),
         ("bias", ctypes.c_void_p),
+        ("ab_dtype", ctypes.c_int),
     ]
 
 
@@ -67,6 +70,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
         lib.tg_gemm.restype = ci
         lib.tg_gemm.argtypes = [vp, ci, i64, vp, ci, i64, vp, ci, i64, i64, i64, i64, ci, vp, vp]
+        lib.tg_gemm_ex.restype = ci
+        lib.tg_gemm_ex.argtypes = [ctypes.POINTER(GroupProblem), vp]
         lib.tg_gemm_bcast.restype = ci
         lib.tg_gemm_bcast.argtypes = [vp, ci, i64, i64, i64, vp, ci, i64, vp, ci, i64, i64, i64, ci, vp, vp]
         lib.tg_grouped_gemm.restype = ci
@@ -83,6 +88,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_set_wait_budget_ms.argtypes = [ctypes.c_uint32]
         lib.tg_debug_withhold_stage.restype = ci
         lib.tg_debug_withhold_stage.argtypes = [i64]
+        lib.tg_debug_trace.restype = ci
+        lib.tg_debug_trace.argtypes = [vp, i64, vp, i64]
         lib.tg_version.restype = ctypes.c_uint32
         lib.tg_version.argtypes = []
         if path is None:
@@ -126,33 +133,39 @@ def _ptr(t) -> int:
 
 def gemm(a: torch.Tensor, b: torch.Tensor, out: torch.Tensor | None = None, *, bias: torch.Tensor | None = None,
          epilogue: str = "none", out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
-    """out[M,N] = epilogue(a[M,K] @ b[K,N]) on the GPU via tg_gemm.
+    """out[M,N] = epilogue(a[M,K] @ b[K,N]) on the GPU (tg_gemm, or tg_gemm_ex for fp16 operands).
 
-    ``a``/``b`` are bf16 CUDA tensors; each may be a row-major or column-major
-    view (a transposed view of a row-major tensor is column-major).  ``out``
-    (bf16 or fp32, rows contiguous, row stride may exceed N) is allocated if
-    not given.  Asynchronous on ``stream`` (default: torch's current stream).
+    ``a``/``b`` are bf16 or fp16 CUDA tensors of the same type (``bias`` too);
+    each may be a row-major or column-major view (a transposed view of a
+    row-major tensor is column-major).  ``out`` (bf16, fp16 or fp32, rows
+    contiguous, row stride may exceed N) is allocated if not given.
+    Asynchronous on ``stream`` (default: torch's current stream).
     """
-    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
-        raise TypeError("a and b must be torch.bfloat16")
+    if a.dtype not in (torch.bfloat16, torch.float16) or b.dtype != a.dtype:
+        raise TypeError("a and b must both be torch.bfloat16 or both torch.float16")
     M, K = a.shape
     K2, N = b.shape
     if K != K2:
         raise ValueError(f"inner dimensions differ: {K} vs {K2}")
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=a.device)
-    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (M, N):
-        raise ValueError("out must be [M, N] bf16 or fp32")
+    if out.dtype not in _DTYPE_CODE or tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N] bf16, fp16 or fp32")
     la, lda = _matrix(a, "a")
     lb, ldb = _matrix(b, "b")
     lc, ldc = _matrix(out, "out")
     if lc != ROW_MAJOR:
         raise ValueError("out must be row-major")
     epi = EPILOGUES[epilogue]
-    if epi and (bias is None or bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_contiguous()):
-        raise ValueError("this epilogue needs a contiguous bf16 bias of length N")
-    _check(load().tg_gemm(_ptr(a), la, lda, _ptr(b), lb, ldb, _ptr(out), F32 if out.dtype == torch.float32 else BF16,
-                          ldc, M, N, K, epi, _ptr(bias) if epi else None, _stream_handle(stream)))
+    if epi and (bias is None or bias.dtype != a.dtype or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("this epilogue needs a contiguous bias of length N with the operands' dtype")
+    if a.dtype == torch.bfloat16:
+        _check(load().tg_gemm(_ptr(a), la, lda, _ptr(b), lb, ldb, _ptr(out), _DTYPE_CODE[out.dtype], ldc, M, N, K,
+                              epi, _ptr(bias) if epi else None, _stream_handle(stream)))
+    else:
+        prob = GroupProblem(M, N, K, _ptr(a), lda, la, _ptr(b), ldb, lb, _ptr(out), ldc, _DTYPE_CODE[out.dtype], epi,
+                            _ptr(bias) if epi else None, F16)
+        _check(load().tg_gemm_ex(ctypes.byref(prob), _stream_handle(stream)))
     return out
 
 
@@ -183,7 +196,7 @@ def gemm_bcast(a_user: torch.Tensor, b: torch.Tensor, repeat: int, out: torch.Te
     if epi and (bias is None or bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_contiguous()):
         raise ValueError("this epilogue needs a contiguous bf16 bias of length N")
     _check(load().tg_gemm_bcast(_ptr(a_user), la, lda, U, repeat, _ptr(b), lb, ldb, _ptr(out),
-                                F32 if out.dtype == torch.float32 else BF16, ldc, N, K, epi,
+                                _DTYPE_CODE[out.dtype], ldc, N, K, epi,
                                 _ptr(bias) if epi else None, _stream_handle(stream)))
     return out
 
@@ -197,8 +210,8 @@ def make_problem(a, b, out, *, bias=None, epilogue="none") -> GroupProblem:
     _, ldc = _matrix(out, "out") if out.numel() else (ROW_MAJOR, max(N, 1))
     epi = EPILOGUES[epilogue]
     return GroupProblem(M, N, K, _ptr(a) if a.numel() else None, lda, la, _ptr(b), ldb, lb,
-                        _ptr(out) if out.numel() else None, ldc, F32 if out.dtype == torch.float32 else BF16, epi,
-                        _ptr(bias) if epi else None)
+                        _ptr(out) if out.numel() else None, ldc, _DTYPE_CODE[out.dtype], epi,
+                        _ptr(bias) if epi else None, F16 if b.dtype == torch.float16 else BF16)
 
 
 def grouped_gemm_table(table, stream=None) -> None:
@@ -256,6 +269,17 @@ def set_wait_budget_ms(ms: int) -> None:
 
 def debug_withhold_stage(k_block: int) -> None:
     _check(load().tg_debug_withhold_stage(k_block))
+
+
+def debug_trace(tile_records: torch.Tensor | None, cta_records: torch.Tensor | None = None) -> None:
+    """Arm a timeline trace of this thread's next launch (see tg_debug_trace in include/tg.h).
+
+    ``tile_records`` is an int64 CUDA tensor [T, 4] and ``cta_records`` [B, 2]."""
+    tp = 0 if tile_records is None else tile_records.data_ptr()
+    tc = 0 if tile_records is None else tile_records.shape[0]
+    cp = 0 if cta_records is None else cta_records.data_ptr()
+    cc = 0 if cta_records is None else cta_records.shape[0]
+    _check(load().tg_debug_trace(tp or None, tc, cp or None, cc))
 
 
 def version() -> tuple[int, int]:

@@ -84,7 +84,7 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
     if failed:
         raise RuntimeError("nvcc failed (see output above)")
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [exe] + ARCH + ["-shared", "-o", tmp] + [obj for _, obj, _ in results]
+    cmd = [exe] + ARCH + ["-shared", "-Xlinker", "--no-undefined", "-o", tmp] + [obj for _, obj, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)

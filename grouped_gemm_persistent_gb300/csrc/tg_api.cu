@@ -40,6 +40,13 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 thread_local std::string t_message;
 thread_local int64_t t_withhold = -1;
+struct TraceArm {
+    uint64_t* tiles = nullptr;
+    int64_t tiles_cap = 0;
+    uint64_t* ctas = nullptr;
+    int64_t ctas_cap = 0;
+};
+thread_local TraceArm t_trace;
 
 std::atomic<uint32_t> g_budget_ms{0};
 
@@ -175,14 +182,23 @@ struct Prob {
     int64_t M, N, K;
     tg_epilogue epi;
     const void* bias;
+    tg_dtype ab;          // element type of A, B and bias: TG_BF16 or TG_F16
 };
+
+Prob prob_of(const tg_group_problem& t) {
+    return Prob{t.A, t.layout_a, t.lda, t.B, t.layout_b, t.ldb, t.C, t.c_dtype, t.ldc, t.M, t.N, t.K, t.epi, t.bias,
+                t.ab_dtype};
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 tg_status check(const Prob& q, int g) {
     if (q.la != TG_ROW_MAJOR && q.la != TG_COL_MAJOR) return fail(TG_ERR_INVALID_ARG, "problem %d: bad layout_a %d", g, int(q.la));
     if (q.lb != TG_ROW_MAJOR && q.lb != TG_COL_MAJOR) return fail(TG_ERR_INVALID_ARG, "problem %d: bad layout_b %d", g, int(q.lb));
-    if (q.cd != TG_BF16 && q.cd != TG_F32) return fail(TG_ERR_INVALID_ARG, "problem %d: bad c_dtype %d", g, int(q.cd));
+    if (q.cd != TG_BF16 && q.cd != TG_F32 && q.cd != TG_F16)
+        return fail(TG_ERR_INVALID_ARG, "problem %d: bad c_dtype %d", g, int(q.cd));
+    if (q.ab != TG_BF16 && q.ab != TG_F16)
+        return fail(TG_ERR_INVALID_ARG, "problem %d: bad ab_dtype %d (A and B are bf16 or fp16)", g, int(q.ab));
     if (q.epi != TG_EPI_NONE && q.epi != TG_EPI_BIAS && q.epi != TG_EPI_BIAS_GELU)
         return fail(TG_ERR_INVALID_ARG, "problem %d: bad epilogue %d", g, int(q.epi));
     if (q.M < 0 || q.N < 0 || q.K < 0)
@@ -208,7 +224,7 @@ tg_status check(const Prob& q, int g) {
         if (!aligned16(q.A) || !aligned16(q.B))
             return fail(TG_ERR_UNSUPPORTED, "problem %d: A and B must be 16-byte aligned (TMA)", g);
         if ((q.lda * 2) % 16 || (q.ldb * 2) % 16)
-            return fail(TG_ERR_UNSUPPORTED, "problem %d: lda and ldb must be multiples of 8 bf16 elements (TMA)", g);
+            return fail(TG_ERR_UNSUPPORTED, "problem %d: lda and ldb must be multiples of 8 elements (TMA)", g);
     }
     const int64_t esize = q.cd == TG_F32 ? 4 : 2;
     if (q.ldc > kMaxDim) return fail(TG_ERR_UNSUPPORTED, "problem %d: ldc must be below 2^31", g);
@@ -303,7 +319,8 @@ int pick_band(int64_t tiles_n, int units) {
 
 tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     std::memset(out, 0, sizeof(Problem));
-    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const bool ab_f16 = q.ab == TG_F16;
+    const CUtensorMapDataType bf16 = ab_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     tg_status s;
     if (q.K > 0) {
         if (q.la == TG_ROW_MAJOR)
@@ -318,10 +335,15 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
         if (s != TG_OK) return s;
     }
     const bool f32 = q.cd == TG_F32;
-    s = make_map(&out->tma_c, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : bf16, q.C, q.N, q.M, q.ldc * (f32 ? 4 : 2),
-                 v.cw, 32, "C", g);
+    const CUtensorMapDataType c_type = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : (q.cd == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+    s = make_map(&out->tma_c, c_type, q.C, q.N, q.M, q.ldc * (f32 ? 4 : 2), v.cw, 32, "C", g);
     if (s != TG_OK) return s;
-    out->bias = static_cast<const __nv_bfloat16*>(q.epi != TG_EPI_NONE ? q.bias : nullptr);
+    out->bias = q.epi != TG_EPI_NONE ? q.bias : nullptr;
+    out->idesc = tg::ptx::idesc_f32_acc(v.tile_m, v.bn, q.la == TG_COL_MAJOR, q.lb == TG_ROW_MAJOR, ab_f16);
+    out->idesc_half = tg::ptx::idesc_f32_acc(v.tile_m, v.bn / 2, q.la == TG_COL_MAJOR, q.lb == TG_ROW_MAJOR, ab_f16);
+    out->flags = (q.cd == TG_F16 ? tg::FLAG_C_F16 : 0u) | (ab_f16 ? tg::FLAG_BIAS_F16 : 0u);
     out->M = static_cast<int32_t>(q.M);
     out->N = static_cast<int32_t>(q.N);
     out->K = static_cast<int32_t>(q.K);
@@ -340,6 +362,11 @@ void base_params(Params* p, DeviceState* d) {
     p->wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
     p->withhold_kb = t_withhold;
     t_withhold = -1;
+    p->trace_tiles = t_trace.tiles;
+    p->trace_tiles_cap = t_trace.tiles_cap;
+    p->trace_ctas = t_trace.ctas;
+    p->trace_ctas_cap = t_trace.ctas_cap;
+    t_trace = TraceArm{};
 }
 
 tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t stream) {
@@ -436,6 +463,10 @@ thread_local tg::Problem t_noalloc_host[TG_NOALLOC_MAX_PROBLEMS];
 
 }  // namespace
 
+namespace {
+tg_status dense_gemm(const Prob& q, tg_stream_t stream);
+}  // namespace
+
 // ========================================================================================
 // C ABI
 
@@ -444,7 +475,23 @@ extern "C" {
 tg_status tg_gemm(const void* A, tg_layout layout_a, int64_t lda, const void* B, tg_layout layout_b, int64_t ldb,
                   void* C, tg_dtype c_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K, tg_epilogue epi,
                   const void* bias, tg_stream_t stream) {
-    const Prob q{A, layout_a, lda, B, layout_b, ldb, C, c_dtype, ldc, M, N, K, epi, bias};
+    return dense_gemm(Prob{A, layout_a, lda, B, layout_b, ldb, C, c_dtype, ldc, M, N, K, epi, bias, TG_BF16}, stream);
+}
+
+tg_status tg_gemm_ex(const tg_group_problem* problem, tg_stream_t stream) {
+    if (!problem) return fail(TG_ERR_INVALID_ARG, "problem is NULL");
+    return dense_gemm(prob_of(*problem), stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+tg_status dense_gemm(const Prob& q, tg_stream_t stream) {
+    const void* B = q.B;
+    const tg_layout layout_a = q.la, layout_b = q.lb;
+    const tg_dtype c_dtype = q.cd;
+    const int64_t ldb = q.ldb, M = q.M, N = q.N, K = q.K;
     tg_status s = check(q, 0);
     if (s != TG_OK) return s;
     if (M == 0 || N == 0) return TG_OK;
@@ -476,14 +523,19 @@ tg_status tg_gemm(const void* A, tg_layout layout_a, int64_t lda, const void* B,
         p.dense.split_begin = static_cast<int32_t>(p.total_tiles - rem);
         p.total_tiles += rem;
         if (layout_b == TG_COL_MAJOR) {
-            if ((s = make_map(&p.dense_b_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, ldb * 2, 64, v.bn_cta / 2,
-                              "B (half-width tiles)", 0)) != TG_OK)
+            if ((s = make_map(&p.dense_b_half, q.ab == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              B, K, N, ldb * 2, 64, v.bn_cta / 2, "B (half-width tiles)", 0)) != TG_OK)
                 return s;
         }
     }
     base_params(&p, d);
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
 }
+
+}  // namespace
+
+extern "C" {
 
 tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int64_t U, int64_t repeat,
                         const void* B, tg_layout layout_b, int64_t ldb, void* C, tg_dtype c_dtype, int64_t ldc,
@@ -493,7 +545,7 @@ tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int
     if (U > 0 && repeat > kMaxDim / U)
         return fail(TG_ERR_UNSUPPORTED, "U * repeat must be below 2^31 (U=%lld, repeat=%lld)", (long long)U,
                     (long long)repeat);
-    const Prob q{A_user, layout_a, lda, B, layout_b, ldb, C, c_dtype, ldc, U, N, K, epi, bias};
+    const Prob q{A_user, layout_a, lda, B, layout_b, ldb, C, c_dtype, ldc, U, N, K, epi, bias, TG_BF16};
     tg_status s = check(q, 0);
     if (s != TG_OK) return s;
     if (U == 0 || N == 0) return TG_OK;
@@ -515,7 +567,9 @@ tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int
     if ((s = fill_problem(q, v, 0, &p.dense)) != TG_OK) return s;
     const bool f32 = c_dtype == TG_F32;
     const uint64_t row = static_cast<uint64_t>(ldc) * (f32 ? 4 : 2);
-    if ((s = make_map_3d(&p.dense.tma_c, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C,
+    if ((s = make_map_3d(&p.dense.tma_c, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                             : (c_dtype == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                  : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16), C,
                          N, repeat, U, row, row * repeat, v.cw, 1, 32, "C (broadcast view)")) != TG_OK)
         return s;
     const int64_t tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
@@ -540,7 +594,7 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
     bool any = false;
     for (int g = 0; g < G; ++g) {
         const tg_group_problem& t = table[g];
-        qs[g] = Prob{t.A, t.layout_a, t.lda, t.B, t.layout_b, t.ldb, t.C, t.c_dtype, t.ldc, t.M, t.N, t.K, t.epi, t.bias};
+        qs[g] = prob_of(t);
         tg_status s = check(qs[g], g);
         if (s != TG_OK) return s;
         any = any || (t.M > 0 && t.N > 0);
@@ -618,7 +672,7 @@ tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_strea
     int live = 0;
     for (int g = 0; g < G; ++g) {
         const tg_group_problem& t = table[g];
-        const Prob q{t.A, t.layout_a, t.lda, t.B, t.layout_b, t.ldb, t.C, t.c_dtype, t.ldc, t.M, t.N, t.K, t.epi, t.bias};
+        const Prob q = prob_of(t);
         tg_status s = check(q, g);
         if (s != TG_OK) return s;
         live += (t.M > 0 && t.N > 0) ? 1 : 0;
@@ -673,7 +727,7 @@ tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_strea
             if (t.M == 0 || t.N == 0) continue;
             const int k2 = (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) + (t.c_dtype == TG_F32 ? 1 : 0);
             if (k2 != key) continue;
-            const Prob q{t.A, t.layout_a, t.lda, t.B, t.layout_b, t.ldb, t.C, t.c_dtype, t.ldc, t.M, t.N, t.K, t.epi, t.bias};
+            const Prob q = prob_of(t);
             if ((s = fill_problem(q, v, g, &host[n])) != TG_OK) return s;
             host[n].tile_begin = tiles;
             tiles += static_cast<int64_t>(host[n].tiles_m) * host[n].tiles_n;
@@ -741,6 +795,15 @@ tg_status tg_set_wait_budget_ms(uint32_t ms) {
 tg_status tg_debug_withhold_stage(int64_t k_block) {
     if (k_block < -1) return fail(TG_ERR_INVALID_ARG, "k_block must be >= -1");
     t_withhold = k_block;
+    return TG_OK;
+}
+
+tg_status tg_debug_trace(uint64_t* tile_records, int64_t tile_capacity, uint64_t* cta_records, int64_t cta_capacity) {
+    if (tile_capacity < 0 || cta_capacity < 0) return fail(TG_ERR_INVALID_ARG, "negative trace capacity");
+    if ((tile_capacity > 0 && !tile_records) || (cta_capacity > 0 && !cta_records))
+        return fail(TG_ERR_INVALID_ARG, "trace buffer is NULL");
+    t_trace = TraceArm{tile_capacity ? tile_records : nullptr, tile_capacity, cta_capacity ? cta_records : nullptr,
+                       cta_capacity};
     return TG_OK;
 }
 

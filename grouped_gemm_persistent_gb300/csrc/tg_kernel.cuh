@@ -36,6 +36,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "tg_ptx.cuh"
@@ -69,7 +70,7 @@ struct alignas(128) Problem {
     CUtensorMap tma_a;
     CUtensorMap tma_b;
     CUtensorMap tma_c;
-    const __nv_bfloat16* bias;
+    const void* bias;       // bf16 or fp16 [N] (FLAG_BIAS_F16)
     int64_t tile_begin;   // global index of this problem's first tile
     int32_t M, N, K;
     int32_t epi;
@@ -86,6 +87,14 @@ struct alignas(128) Problem {
     // takes half a tile time.  Half tile u covers full tile split_begin + u/2,
     // columns [BN/2 * (u % 2), BN/2 * (u % 2 + 1)).  INT32_MAX: no split.
     int32_t split_begin;
+    uint32_t idesc;             // tcgen05 instruction descriptor of a full-width tile (operand types, M, N, majors)
+    uint32_t idesc_half;        // the same for a half-width tile
+    uint32_t flags;             // FLAG_*: 16-bit output and bias element types
+};
+
+enum : uint32_t {
+    FLAG_C_F16 = 1u,      // 16-bit output is IEEE fp16 (else bf16)
+    FLAG_BIAS_F16 = 2u,   // bias is fp16 (else bf16)
 };
 
 struct Params {
@@ -98,6 +107,14 @@ struct Params {
     ErrorRecord* err;
     uint64_t wait_budget_ns;
     int64_t withhold_kb;        // test hook, -1 = off (see tg_debug_withhold_stage)
+    // Timeline trace (tg_debug_trace), null when off.  trace_tiles[t] = {block,
+    // first k-block ready, accumulator complete, epilogue done} for global tile
+    // t < trace_tiles_cap (times from %globaltimer, ns); trace_ctas[b] =
+    // {set-up done, teardown start} for block b < trace_ctas_cap.
+    uint64_t* trace_tiles;
+    int64_t trace_tiles_cap;
+    uint64_t* trace_ctas;
+    int64_t trace_ctas_cap;
 };
 
 template <int BN_, int CTA_GROUP_, bool A_MN_, bool B_MN_, bool C_F32_, bool GROUPED_>
@@ -132,8 +149,6 @@ struct Config {
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 
-    static constexpr uint32_t IDESC = ptx::idesc_bf16_f32(TILE_M, BN, A_MN, B_MN);
-    static constexpr uint32_t IDESC_HALF = ptx::idesc_bf16_f32(TILE_M, BN / 2, A_MN, B_MN);
     static constexpr bool CAN_SPLIT = (BN_CTA / 2) % 64 == 0;   // half-width B still in whole 64-column boxes
 
     static_assert(BN == 128 || BN == 256, "tile width");
@@ -291,6 +306,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
 // ----------------------------------------------------------------------------------------
 // the kernel
 
@@ -354,6 +374,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_TMEM_SLOT);
+    if (p.trace_ctas && threadIdx.x == 0 && blockIdx.x < p.trace_ctas_cap)
+        p.trace_ctas[2 * blockIdx.x] = ptx::globaltimer_ns();
 
     if (warp == 0) {
         // ================================ TMA producer ================================
@@ -447,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 g = find_problem<Cfg>(p, t, g);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
-                const uint32_t idesc = tc.width == Cfg::BN ? Cfg::IDESC : Cfg::IDESC_HALF;
+                const uint32_t idesc = tc.width == Cfg::BN ? pr.idesc : pr.idesc_half;
                 if (!wait_bounded<CG>(tempty_bar(acc), acc_phase ^ 1u, p, abort_addr, ROLE_MMA, t, 16 + acc)) {
                     aborted = true;
                     break;
@@ -460,6 +482,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         break;
                     }
                     ptx::tc_fence_after_sync();
+                    if (kb == 0 && p.trace_tiles && t < p.trace_tiles_cap) {
+                        p.trace_tiles[4 * t + 0] = blockIdx.x;
+                        p.trace_tiles[4 * t + 1] = ptx::globaltimer_ns();
+                    }
                     const uint32_t a_addr = sA + stage * Cfg::A_BYTES;
                     const uint32_t b_addr = sB + stage * Cfg::B_BYTES;
                     const uint64_t a_desc = Cfg::A_MN ? ptx::smem_desc_sw128(a_addr, 8192, 1024)
@@ -503,7 +529,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const int ew = warp - EPI_WARP0;                     // 0..3
         const int q = warp % 4;                              // TMEM lane quarter this warp may read
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        __nv_bfloat16* bias_s = reinterpret_cast<__nv_bfloat16*>(smem + Cfg::OFF_BIAS) + ew * BN;
+        uint16_t* bias_s = reinterpret_cast<uint16_t*>(smem + Cfg::OFF_BIAS) + ew * BN;   // raw bf16 / fp16 bits
         const uint32_t c_stage0 = sC + ew * 2 * C_STAGE_BYTES;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -525,9 +551,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             // bias of this tile's columns into this warp's slot (zeros past N)
             if (epi != EPI_NONE && active) {
+                const uint16_t* bias_g = reinterpret_cast<const uint16_t*>(pr.bias);
                 for (int i = lane; i < BN; i += 32) {
                     const int n = tc.n0 + i;
-                    bias_s[i] = (n < pr.N) ? pr.bias[n] : __float2bfloat16_rn(0.0f);
+                    bias_s[i] = (n < pr.N) ? bias_g[n] : uint16_t(0);   // +0 in both encodings
                 }
             }
 
@@ -537,6 +564,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             if (!ok) break;
             ptx::tc_fence_after_sync();
             __syncwarp();
+            const bool tracer = p.trace_tiles && lane == 0 && ew == 0 && leader && t < p.trace_tiles_cap;
+            if (tracer) p.trace_tiles[4 * t + 2] = ptx::globaltimer_ns();
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             const int CHUNKS = tc.width / Cfg::CW;
@@ -569,9 +598,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 if (!active || n_chunk >= pr.N) continue;
 
                 if (epi != EPI_NONE) {
-                    const __nv_bfloat16* bs = bias_s + c * Cfg::CW;
+                    const uint16_t* bs = bias_s + c * Cfg::CW;
+                    if (pr.flags & FLAG_BIAS_F16) {
 #pragma unroll
-                    for (int i = 0; i < Cfg::CW; ++i) v[i] += __bfloat162float(bs[i]);
+                        for (int i = 0; i < Cfg::CW; ++i) v[i] += __half2float(__ushort_as_half(bs[i]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < Cfg::CW; ++i) v[i] += __uint_as_float(static_cast<uint32_t>(bs[i]) << 16);
+                    }
                     if (epi == EPI_BIAS_GELU) {
 #pragma unroll
                         for (int i = 0; i < Cfg::CW; ++i) v[i] = gelu_tanh_f32(v[i]);
@@ -583,6 +617,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 if (lane == 0) ptx::bulk_wait_group_read<1>();
                 __syncwarp();
                 const uint32_t row_addr = buf + lane * 128;
+                const bool c_f16 = (pr.flags & FLAG_C_F16) != 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint32_t w0, w1, w2, w3;
@@ -591,6 +626,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         w1 = __float_as_uint(v[4 * j + 1]);
                         w2 = __float_as_uint(v[4 * j + 2]);
                         w3 = __float_as_uint(v[4 * j + 3]);
+                    } else if (c_f16) {
+                        w0 = pack_f16x2(v[8 * j + 0], v[8 * j + 1]);
+                        w1 = pack_f16x2(v[8 * j + 2], v[8 * j + 3]);
+                        w2 = pack_f16x2(v[8 * j + 4], v[8 * j + 5]);
+                        w3 = pack_f16x2(v[8 * j + 6], v[8 * j + 7]);
                     } else {
                         w0 = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
                         w1 = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
@@ -616,6 +656,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 }
                 sbuf ^= 1;
             }
+            if (tracer) p.trace_tiles[4 * t + 3] = ptx::globaltimer_ns();
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
@@ -624,6 +665,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
     // ---- teardown (lanes 1-31 of warps 0 and 1 wait here for their lane 0)
     __syncwarp();
+    if (p.trace_ctas && warp == EPI_WARP0 && lane == 0 && blockIdx.x < p.trace_ctas_cap)
+        p.trace_ctas[2 * blockIdx.x + 1] = ptx::globaltimer_ns();
     ptx::tc_fence_before_sync();
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after_sync();

@@ -249,12 +249,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_
     return d;
 }
 
-// Instruction descriptor for tcgen05.mma.kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32)   bits 7-9 A format (1 = bf16)   bits 10-12 B format (1 = bf16)
+// Instruction descriptor for tcgen05.mma.kind::f16 with an fp32 accumulator.
+//   bits 4-5 D format (1 = f32)   bits 7-9 A format, bits 10-12 B format (0 = f16, 1 = bf16)
 //   bit 15 A is MN-major          bit 16 B is MN-major
 //   bits 17-22 N >> 3             bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) |
+__host__ __device__ constexpr uint32_t idesc_f32_acc(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major,
+                                                     bool operands_f16) {
+    return (1u << 4) | ((operands_f16 ? 0u : 1u) << 7) | ((operands_f16 ? 0u : 1u) << 10) |
            (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }

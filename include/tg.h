@@ -70,8 +70,9 @@ typedef enum {
 } tg_layout;
 
 typedef enum {
-    TG_BF16 = 0,  /* output rounded once, to nearest even, from the fp32 epilogue value */
-    TG_F32 = 1    /* output is the fp32 epilogue value itself */
+    TG_BF16 = 0,  /* bfloat16; as output, rounded once to nearest even from the fp32 epilogue value */
+    TG_F32 = 1,   /* output only: the fp32 epilogue value itself */
+    TG_F16 = 2    /* IEEE binary16 (the TLX listing's type); as output, rounded once to nearest even */
 } tg_dtype;
 
 /*
@@ -80,7 +81,7 @@ typedef enum {
  *   A, layout_a, lda : bf16 M x K.  Row-major: lda >= K.  Column-major: lda >= M.
  *   B, layout_b, ldb : bf16 K x N.  Row-major: ldb >= N.  Column-major (i.e. the
  *                      N x K matrix B^T stored row-major): ldb >= K.
- *   C, c_dtype, ldc  : M x N, always row-major, ldc >= N, bf16 or fp32.
+ *   C, c_dtype, ldc  : M x N, always row-major, ldc >= N, bf16, fp32 or fp16.
  *   epi, bias        : bias is a device bf16[N] (2-byte aligned); required for
  *                      TG_EPI_BIAS / TG_EPI_BIAS_GELU, ignored for TG_EPI_NONE.
  *   A and B may be NULL only when K == 0.  C must not overlap A, B or bias.
@@ -130,10 +131,19 @@ typedef struct tg_group_problem {
     int64_t M, N, K;
     const void *A;  int64_t lda; tg_layout layout_a;
     const void *B;  int64_t ldb; tg_layout layout_b;
-    void *C;        int64_t ldc; tg_dtype c_dtype;
+    void *C;        int64_t ldc; tg_dtype c_dtype;   /* TG_BF16, TG_F32 or TG_F16 */
     tg_epilogue epi;
     const void *bias;
+    tg_dtype ab_dtype;  /* element type of A, B and bias: TG_BF16 (0, the default) or TG_F16 */
 } tg_group_problem;
+
+/*
+ * tg_gemm_ex - one dense GEMM described by a problem record (fields as for
+ * tg_gemm), which also selects fp16 operands (ab_dtype = TG_F16, the element
+ * type of the TLX listing) and an fp16 output (c_dtype = TG_F16).  The record
+ * is read during the call only.
+ */
+tg_status tg_gemm_ex(const tg_group_problem *problem, tg_stream_t stream);
 
 /*
  * tg_grouped_gemm - G independent GEMMs in one persistent launch (one launch
@@ -216,6 +226,22 @@ tg_status tg_set_wait_budget_ms(uint32_t ms);
  * disables it; the hook disarms itself after one launch.  Nothing faults.
  */
 tg_status tg_debug_withhold_stage(int64_t k_block);
+
+/*
+ * Timeline trace of the next launch made by this thread (a profiling aid; off
+ * by default, disarms itself after one launch).  Both buffers are DEVICE
+ * memory owned by the caller; the kernel writes, with %globaltimer nanosecond
+ * stamps:
+ *   tile_records[4 t .. 4 t + 3] for global tile t < tile_capacity:
+ *       {block index, first k-block ready for the MMA, accumulator complete,
+ *        epilogue done} (tile order as scheduled: unit u runs tiles u, u + U, ...);
+ *   cta_records[2 b .. 2 b + 1] for block b < cta_capacity:
+ *       {set-up done, teardown start}.
+ * Capacities may be 0 to skip a buffer.  Grouped calls with several layout
+ * classes trace only their first launch.
+ */
+tg_status tg_debug_trace(uint64_t *tile_records, int64_t tile_capacity,
+                         uint64_t *cta_records, int64_t cta_capacity);
 
 /* Library version as (major << 16) | minor. */
 uint32_t tg_version(void);

@@ -114,10 +114,25 @@ def test_grouped_table_checks(lib):
 
 
 def test_struct_layout_matches_header():
-    # natural layout of tg_group_problem on LP64: 13 fields, 104 bytes
-    assert ctypes.sizeof(_binding.GroupProblem) == 104
+    # natural layout of tg_group_problem on LP64: 14 fields, 112 bytes
+    assert ctypes.sizeof(_binding.GroupProblem) == 112
     assert _binding.GroupProblem.bias.offset == 96
     assert _binding.GroupProblem.epi.offset == 92
+    assert _binding.GroupProblem.ab_dtype.offset == 104
+
+
+def test_gemm_ex_checks(lib):
+    P = _binding.GroupProblem
+    good = P(64, 64, 64, ALIGNED, 64, 0, ALIGNED_B, 64, 0, ALIGNED_C, 64, 2, 0, None, 2)   # fp16 in, fp16 out
+    assert lib.tg_gemm_ex(None, None) == tg.TG_ERR_INVALID_ARG
+    bad_ab = P(64, 64, 64, ALIGNED, 64, 0, ALIGNED_B, 64, 0, ALIGNED_C, 64, 0, 0, None, 1)  # fp32 operands
+    assert lib.tg_gemm_ex(ctypes.byref(bad_ab), None) == tg.TG_ERR_INVALID_ARG
+    assert b"ab_dtype" in lib.tg_last_error_message()
+    bad_c = P(64, 64, 64, ALIGNED, 64, 0, ALIGNED_B, 64, 0, ALIGNED_C, 64, 3, 0, None, 0)
+    assert lib.tg_gemm_ex(ctypes.byref(bad_c), None) == tg.TG_ERR_INVALID_ARG
+    empty = P(0, 64, 64, None, 64, 0, None, 64, 0, None, 64, 2, 0, None, 2)
+    assert lib.tg_gemm_ex(ctypes.byref(empty), None) == tg.TG_OK
+    assert good.ab_dtype == 2
 
 
 def test_hooks_validate(lib):

@@ -197,6 +197,66 @@ def test_side_stream():
     check_dense(case, c)
 
 
+# ------------------------------------------------------------------------------------------ fp16 operands
+
+def _f16_case(M, N, K, seed, a_col, b_col, scale=0.25, ints=False):
+    gen = torch.Generator().manual_seed(seed)
+    def draw(shape):
+        if ints:
+            return torch.randint(-4, 5, shape, generator=gen).to(torch.float16)
+        return (torch.randn(shape, generator=gen) * scale).to(torch.float16)
+    a = draw((K, M) if a_col else (M, K))
+    b = draw((N, K) if b_col else (K, N))
+    bias = (torch.randn(N, generator=gen) * 0.1).to(torch.float16)
+    return a, b, bias
+
+
+@pytest.mark.parametrize("a_col,b_col", LAYOUTS)
+@pytest.mark.parametrize("epi", ["none", "bias_gelu"])
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_f16_operands(a_col, b_col, epi, out_dtype, tile):
+    M, N, K = 264, 392, 200
+    a, b, bias = _f16_case(M, N, K, 61, a_col, b_col)
+    da, db = a.cuda(), b.cuda()
+    out = tg.gemm(da.t() if a_col else da, db.t() if b_col else db, bias=bias.cuda(), epilogue=epi, out_dtype=out_dtype)
+    _sync_ok()
+    h = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    y, s = oracle.gemm(h(a), h(b), a_col_major=a_col, b_col_major=b_col, bias=h(bias), epi=epi, in_dtype="f16")
+    r = oracle.compare(to_f64(out), y, s, np.abs(bias.double().numpy()) if epi != "none" else None)
+    assert r["ok"] and r["max_tight"] < 4.0, r
+
+
+def test_f16_integer_exact(tile, split):
+    a, b, _ = _f16_case(300, 264, 640, 62, False, True, ints=True)
+    out = tg.gemm(a.cuda(), b.cuda().t(), out_dtype=torch.float32)
+    _sync_ok()
+    exact = (a.double() @ b.double().t()).numpy()
+    assert np.array_equal(to_f64(out), exact)
+    out16 = tg.gemm(a.cuda(), b.cuda().t(), out_dtype=torch.float16)
+    _sync_ok()
+    assert torch.equal(out16.cpu().view(torch.int16), torch.from_numpy(exact).to(torch.float16).view(torch.int16))
+
+
+def test_grouped_mixed_bf16_and_f16_problems(tile):
+    gen = torch.Generator().manual_seed(63)
+    keep, probs, refs = [], [], []
+    for M, N, K, dt in [(100, 136, 64, torch.float16), (257, 264, 200, torch.bfloat16), (64, 136, 128, torch.float16)]:
+        a = (torch.randn((M, K), generator=gen) / 4).to(dt)
+        b = (torch.randn((K, N), generator=gen) / 4).to(dt)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        da, db = a.cuda(), b.cuda()
+        keep += [da, db, out]
+        probs.append(tg.make_problem(da, db, out))
+        refs.append((a, b, out, "f16" if dt == torch.float16 else "bf16"))
+    tg.grouped_gemm_table(probs)
+    _sync_ok()
+    for a, b, out, ind in refs:
+        h = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        y, s = oracle.gemm(h(a), h(b), in_dtype=ind)
+        r = oracle.compare(to_f64(out), y, s)
+        assert r["ok"] and r["max_tight"] < 4.0, r
+
+
 # ------------------------------------------------------------------------------------------ in-kernel broadcast
 
 @pytest.mark.parametrize("U,repeat,N,K", [(37, 5, 136, 72), (300, 1, 264, 128), (5, 300, 128, 64),
@@ -329,6 +389,34 @@ def test_bounded_wait_reports_timeout_and_context_survives(tile):
     c = run_dense(case)
     _sync_ok()
     check_dense(case, c)
+
+
+# ------------------------------------------------------------------------------------------ timeline trace
+
+def test_timeline_trace_records_every_tile(tile):
+    case = wl.dense_random(1000, 1000, 512, seed=31, dist="normal")
+    a, b = case.a.cuda(), case.b.cuda()
+    tiles = torch.zeros((4096, 4), dtype=torch.int64, device="cuda")
+    ctas = torch.zeros((1024, 2), dtype=torch.int64, device="cuda")
+    tg.debug_trace(tiles, ctas)
+    c = tg.gemm(a, b)
+    _sync_ok()
+    check_dense(case, c)
+    tr = tiles.cpu().numpy()
+    used = tr[:, 1] > 0
+    n = int(used.sum())
+    assert n > 0 and used[:n].all() and not used[n:].any(), "tiles are traced densely from index 0"
+    t = tr[:n]
+    assert (t[:, 1] <= t[:, 2]).all() and (t[:, 2] <= t[:, 3]).all()
+    cr = ctas.cpu().numpy()
+    live = cr[:, 0] > 0
+    assert live.any() and (cr[live, 0] <= cr[live, 1]).all()
+    assert set(t[:, 0].tolist()) <= set(np.flatnonzero(live).tolist())
+    # the trace disarms itself: a second launch leaves a fresh buffer untouched
+    tiles2 = torch.zeros_like(tiles)
+    tg.gemm(a, b)
+    _sync_ok()
+    assert not tiles2.any()
 
 
 # ------------------------------------------------------------------------------------------ full-size workloads
