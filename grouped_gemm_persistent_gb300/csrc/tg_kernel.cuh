@@ -257,14 +257,25 @@ __device__ __forceinline__ bool abort_raised(uint32_t abort_addr) {
 
 // Wait for phase `parity` of `bar`.  false: the budget ran out (recorded) or
 // another role aborted; the caller leaves its loop.
-template <int CTA_GROUP>
+//
+// SLEEP waiters (everyone but the MMA issuer) let the hardware suspend them
+// inside try_wait until the phase completes (up to SLEEP_NS per call): a
+// spinning warp would take issue slots from the MMA-issuing warp on the same
+// SM sub-partition and leave the tensor pipe idle between instructions.
+constexpr uint32_t SLEEP_NS = 20000;
+
+template <int CTA_GROUP, bool SLEEP = true>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& p, uint32_t abort_addr,
                                              uint32_t role, int64_t tile, uint32_t stage) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto try_once = [&]() {
+        if constexpr (SLEEP) return ptx::mbar_try_wait_sleep(bar, parity, SLEEP_NS);
+        else return ptx::mbar_try_wait(bar, parity);
+    };
+    if (try_once()) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if ((it & 15u) == 0u) {
+        if (try_once()) return true;
+        if (SLEEP || (it & 15u) == 0u) {
             if (abort_raised(abort_addr)) return false;
             const uint64_t dt = ptx::globaltimer_ns() - t0;
             if (dt > p.wait_budget_ns) {
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < pr.k_blocks; ++kb) {
-                    if (!wait_bounded<CG>(full_bar(stage), phase, p, abort_addr, ROLE_MMA, t, stage)) {
+                    if (!wait_bounded<CG, false>(full_bar(stage), phase, p, abort_addr, ROLE_MMA, t, stage)) {
                         aborted = true;
                         break;
                     }
