@@ -468,7 +468,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
-        if (lane == 0 && leader) {
+        // The whole warp runs the loop, converged; lane 0 issues the MMAs and commits.
+        if (leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -476,64 +477,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             int g = 0;
             bool aborted = false;
             bool any_mma = false;
+            // shared-memory descriptors of stage 0 (A and B)
+            const uint64_t a_desc0 = Cfg::A_MN ? ptx::smem_desc_sw128(sA, 8192, 1024) : ptx::smem_desc_sw128(sA, 16, 1024);
+            const uint64_t b_desc0 = Cfg::B_MN ? ptx::smem_desc_sw128(sB, 8192, 1024) : ptx::smem_desc_sw128(sB, 16, 1024);
+            // Warp-uniform bounded wait: every lane polls once; if the phase is not yet
+            // complete, lane 0 runs the bounded wait and tells the others how it ended.
+            auto warp_wait = [&](uint32_t bar, uint32_t par, int64_t tile, uint32_t st) -> bool {
+                if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, par))) return true;
+                uint32_t ok = 1;
+                if (lane == 0) ok = wait_bounded<CG, false>(bar, par, p, abort_addr, ROLE_MMA, tile, st) ? 1u : 0u;
+                return __shfl_sync(0xffffffffu, ok, 0) != 0;
+            };
             for (int64_t t = unit; t < p.total_tiles && !aborted; t += num_units) {
                 g = find_problem<Cfg>(p, t, g);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
                 const uint32_t idesc = tc.width == Cfg::BN ? pr.idesc : pr.idesc_half;
-                if (!wait_bounded<CG>(tempty_bar(acc), acc_phase ^ 1u, p, abort_addr, ROLE_MMA, t, 16 + acc)) {
+                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, t, 16 + acc)) {
                     aborted = true;
                     break;
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < pr.k_blocks; ++kb) {
-                    if (!wait_bounded<CG, false>(full_bar(stage), phase, p, abort_addr, ROLE_MMA, t, stage)) {
+                const int k_blocks = pr.k_blocks;
+                const bool trace_tile = p.trace_tiles != nullptr && t < p.trace_tiles_cap;
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!warp_wait(full_bar(stage), phase, t, stage)) {
                         aborted = true;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    if (kb == 0 && p.trace_tiles && t < p.trace_tiles_cap) {
-                        p.trace_tiles[4 * t + 0] = blockIdx.x;
-                        p.trace_tiles[4 * t + 1] = ptx::globaltimer_ns();
-                    }
-                    const uint32_t a_addr = sA + stage * Cfg::A_BYTES;
-                    const uint32_t b_addr = sB + stage * Cfg::B_BYTES;
-                    const uint64_t a_desc = Cfg::A_MN ? ptx::smem_desc_sw128(a_addr, 8192, 1024)
-                                                      : ptx::smem_desc_sw128(a_addr, 16, 1024);
-                    const uint64_t b_desc = Cfg::B_MN ? ptx::smem_desc_sw128(b_addr, 8192, 1024)
-                                                      : ptx::smem_desc_sw128(b_addr, 16, 1024);
+                    if (lane == 0) {
+                        if (kb == 0 && trace_tile) {
+                            p.trace_tiles[4 * t + 0] = blockIdx.x;
+                            p.trace_tiles[4 * t + 1] = ptx::globaltimer_ns();
+                        }
+                        // stage s starts s * BYTES further on: add (s * BYTES) >> 4 to the start-address field
+                        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * Cfg::A_BYTES) >> 4);
+                        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // K-major: the next 16 K elements are 32 bytes further along the
-                        // swizzled row; MN-major: 16 rows (2048 bytes) further down.
-                        const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
-                        const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
-                        ptx::mma_bf16<CG>(d_tmem, a_desc + a_off, b_desc + b_off, idesc,
-                                          (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            // K-major: the next 16 K elements are 32 bytes further along the
+                            // swizzled row; MN-major: 16 rows (2048 bytes) further down.
+                            const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
+                            const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
+                            ptx::mma_bf16<CG>(d_tmem, a_desc + a_off, b_desc + b_off, idesc,
+                                              (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if constexpr (CG == 2) ptx::mma_commit_pair(empty_bar(stage), 0x3);
+                        else ptx::mma_commit(empty_bar(stage));
                     }
+                    __syncwarp();
                     any_mma = true;
-                    if constexpr (CG == 2) ptx::mma_commit_pair(empty_bar(stage), 0x3);
-                    else ptx::mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (aborted) break;
-                if (pr.k_blocks > 0) {
-                    if constexpr (CG == 2) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
-                    else ptx::mma_commit(tfull_bar(acc));
-                } else {
-                    // K == 0: nothing to accumulate; the epilogue writes epilogue(0).
-                    ptx::mbar_arrive(tfull_bar(acc));
-                    if constexpr (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa(tfull_bar(acc), 1));
+                if (lane == 0) {
+                    if (k_blocks > 0) {
+                        if constexpr (CG == 2) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
+                        else ptx::mma_commit(tfull_bar(acc));
+                    } else {
+                        // K == 0: nothing to accumulate; the epilogue writes epilogue(0).
+                        ptx::mbar_arrive(tfull_bar(acc));
+                        if constexpr (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa(tfull_bar(acc), 1));
+                    }
                 }
+                __syncwarp();
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
-            if (aborted && any_mma) {
+            if (aborted && any_mma && lane == 0) {
                 // Drain: one more commit completes when every MMA issued so far has.
                 if constexpr (CG == 2) ptx::mma_commit_pair(drain_bar, 0x1);
                 else ptx::mma_commit(drain_bar);
                 if (!wait_quiet(drain_bar, 0, p.wait_budget_ns)) report_timeout(p, ROLE_DRAIN, -1, 0, p.wait_budget_ns);
             }
+            __syncwarp();
         }
     } else {
         // ================================ epilogue ================================

@@ -196,7 +196,9 @@ __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T, bf16 x bf16 -> fp32, shapes from the instruction descriptor.
+// D[tmem] (+)= A[smem] . B[smem]^T with an fp32 accumulator, shapes from the instruction
+// descriptor.  No "memory" clobber: the MMA touches no memory the compiler tracks, and
+// volatile asm keeps its order relative to the barrier waits and commits around it.
 template <int CTA_GROUP>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -205,25 +207,25 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
             "{\n\t.reg .pred p;\n\t"
             "setp.ne.u32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
     else
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
             "setp.ne.u32 p, %4, 0;\n\t"
             "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Arrive once on `bar` (this CTA) when all MMAs issued so far by this thread are complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 :: "r"(bar) : "memory");
+                 :: "r"(bar));
 }
 
 // Same for a CTA pair: arrive on the barrier at offset `bar` in every CTA named by `cta_mask`.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-                 :: "r"(bar), "h"(cta_mask) : "memory");
+                 :: "r"(bar), "h"(cta_mask));
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane (base lane + t).
