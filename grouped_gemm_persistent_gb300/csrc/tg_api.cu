@@ -342,7 +342,6 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     if (s != TG_OK) return s;
     out->bias = q.epi != TG_EPI_NONE ? q.bias : nullptr;
     out->idesc = tg::ptx::idesc_f32_acc(v.tile_m, v.bn, q.la == TG_COL_MAJOR, q.lb == TG_ROW_MAJOR, ab_f16);
-    out->idesc_half = tg::ptx::idesc_f32_acc(v.tile_m, v.bn / 2, q.la == TG_COL_MAJOR, q.lb == TG_ROW_MAJOR, ab_f16);
     out->flags = (q.cd == TG_F16 ? tg::FLAG_C_F16 : 0u) | (ab_f16 ? tg::FLAG_BIAS_F16 : 0u);
     out->M = static_cast<int32_t>(q.M);
     out->N = static_cast<int32_t>(q.N);
@@ -353,7 +352,6 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     out->k_blocks = static_cast<int32_t>((q.K + tg::BK - 1) / tg::BK);
     out->repeat = 0;
     out->replicas = 1;
-    out->split_begin = INT32_MAX;
     return TG_OK;
 }
 
@@ -514,21 +512,6 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream) {
     p.num_problems = 1;
     p.total_tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
     p.band = pick_band(p.dense.tiles_n, units);
-    // A last wave at most half full is split into half-width tiles, so it takes
-    // half a tile time (TG_SPLIT_TAIL=0 turns this off).
-    const int64_t rem = p.total_tiles % units;
-    const char* split_env = std::getenv("TG_SPLIT_TAIL");
-    const bool split_ok = !(split_env && split_env[0] == '0') && v.bn == 256 && v.bn_cta / 2 % 64 == 0;
-    if (split_ok && rem > 0 && 2 * rem <= units && K > 0) {
-        p.dense.split_begin = static_cast<int32_t>(p.total_tiles - rem);
-        p.total_tiles += rem;
-        if (layout_b == TG_COL_MAJOR) {
-            if ((s = make_map(&p.dense_b_half, q.ab == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                              B, K, N, ldb * 2, 64, v.bn_cta / 2, "B (half-width tiles)", 0)) != TG_OK)
-                return s;
-        }
-    }
     base_params(&p, d);
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
 }

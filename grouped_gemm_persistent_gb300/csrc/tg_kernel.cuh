@@ -82,13 +82,7 @@ struct alignas(128) Problem {
     // [r * repeat / replicas, (r + 1) * repeat / replicas).
     int32_t repeat;
     int32_t replicas;           // >= 1
-    // Local tile indices >= split_begin are half-width tiles (BN/2 columns): the
-    // last, partly filled wave of a dense launch is split in two along N so it
-    // takes half a tile time.  Half tile u covers full tile split_begin + u/2,
-    // columns [BN/2 * (u % 2), BN/2 * (u % 2 + 1)).  INT32_MAX: no split.
-    int32_t split_begin;
-    uint32_t idesc;             // tcgen05 instruction descriptor of a full-width tile (operand types, M, N, majors)
-    uint32_t idesc_half;        // the same for a half-width tile
+    uint32_t idesc;             // tcgen05 instruction descriptor (operand types, M, N, majors)
     uint32_t flags;             // FLAG_*: 16-bit output and bias element types
 };
 
@@ -99,7 +93,6 @@ enum : uint32_t {
 
 struct Params {
     Problem dense;              // the problem of a dense launch (lives in parameter space)
-    CUtensorMap dense_b_half;   // B map with a BN_CTA/2-row box, for half-width tiles of column-major B
     const Problem* problems;    // grouped launch: device array written by the host
     int32_t num_problems;
     int32_t band;               // raster band width in N-tiles
@@ -133,23 +126,20 @@ struct Config {
     static constexpr int CW = C_F32 ? 32 : 64;       // output columns per 128-byte staged row
     static constexpr int TMEM_COLS = 2 * BN;         // two fp32 accumulators of BN columns
     static constexpr int C_BYTES = NUM_EPI_WARPS * 2 * C_STAGE_BYTES;
-    static constexpr int BIAS_BYTES = NUM_EPI_WARPS * BN * 2;
-    static constexpr int FIXED = C_BYTES + BIAS_BYTES + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+    static constexpr int FIXED = C_BYTES + 512 /*barriers and slots*/ + 1024 /*alignment slack*/;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_BIAS = OFF_C + C_BYTES;
-    static constexpr int OFF_BAR = OFF_BIAS + BIAS_BYTES;
+    static constexpr int OFF_BAR = OFF_C + C_BYTES;
     // barriers: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
 
-    static constexpr bool CAN_SPLIT = (BN_CTA / 2) % 64 == 0;   // half-width B still in whole 64-column boxes
 
     static_assert(BN == 128 || BN == 256, "tile width");
     static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "cta group");
@@ -168,7 +158,6 @@ struct TileCoord {
     int m0;       // first accumulator row of this CTA
     int n0;       // first column of the tile
     int r;        // replica index (broadcast form), else 0
-    int width;    // tile columns: BN, or BN/2 for a split tail tile
 };
 
 template <class Cfg>
@@ -197,12 +186,6 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
         replica = static_cast<int>(local % pr.replicas);
         local /= pr.replicas;
     }
-    int half = -1;
-    if (local >= pr.split_begin) {
-        const int64_t u = local - pr.split_begin;
-        local = pr.split_begin + u / 2;
-        half = static_cast<int>(u & 1);
-    }
     const int band = p.band;
     const int64_t per_band = static_cast<int64_t>(pr.tiles_m) * band;
     const int b = static_cast<int>(local / per_band);
@@ -216,11 +199,6 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     c.m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
     c.n0 = nb * Cfg::BN;
     c.r = replica;
-    c.width = Cfg::BN;
-    if (half >= 0) {
-        c.width = Cfg::BN / 2;
-        c.n0 += half * (Cfg::BN / 2);
-    }
     return c;
 }
 
@@ -408,14 +386,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     }
                 }
                 const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
-                const bool full_width = tc.width == Cfg::BN;
-                const int b_cols = full_width ? Cfg::BN_CTA : Cfg::BN_CTA / 2;    // B columns this CTA loads
-                const int nb0 = tc.n0 + static_cast<int>(rank) * b_cols;
-                const uint32_t stage_bytes = Cfg::A_BYTES + (full_width ? Cfg::B_BYTES : Cfg::B_BYTES / 2);
-                const CUtensorMap* b_map = &pr.tma_b;
-                if constexpr (!Cfg::GROUPED && !Cfg::B_MN) {
-                    if (!full_width) b_map = &p.dense_b_half;
-                }
+                const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // first B column this CTA loads
                 for (int kb = 0; kb < pr.k_blocks; ++kb) {
                     if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, t, stage)) {
                         aborted = true;
@@ -424,7 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     const bool skip = withhold && kb == p.withhold_kb;
                     if (!skip) {
                         const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
-                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_bytes * CG);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES * CG);
                         const int k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * Cfg::A_BYTES;
                         const uint32_t b_dst = sB + stage * Cfg::B_BYTES;
@@ -439,9 +410,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             load(a_dst, &pr.tma_a, k0, tc.m0);
                         }
                         if constexpr (Cfg::B_MN) {
-                            for (int j = 0; j < b_cols / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+#pragma unroll
+                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
                         } else {
-                            load(b_dst, b_map, k0, nb0);
+                            load(b_dst, &pr.tma_b, k0, nb0);
                         }
                         ++issued;
                     }
@@ -491,8 +463,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             for (int64_t t = unit; t < p.total_tiles && !aborted; t += num_units) {
                 g = find_problem<Cfg>(p, t, g);
                 const Problem& pr = problem_of<Cfg>(p, g);
-                const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
-                const uint32_t idesc = tc.width == Cfg::BN ? pr.idesc : pr.idesc_half;
+                const uint32_t idesc = pr.idesc;
                 if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, t, 16 + acc)) {
                     aborted = true;
                     break;
@@ -558,7 +529,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         const int ew = warp - EPI_WARP0;                     // 0..3
         const int q = warp % 4;                              // TMEM lane quarter this warp may read
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-        uint16_t* bias_s = reinterpret_cast<uint16_t*>(smem + Cfg::OFF_BIAS) + ew * BN;   // raw bf16 / fp16 bits
         const uint32_t c_stage0 = sC + ew * 2 * C_STAGE_BYTES;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -578,14 +548,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             const bool active = row0 < pr.M;
             const int epi = pr.epi;
 
-            // bias of this tile's columns into this warp's slot (zeros past N)
-            if (epi != EPI_NONE && active) {
-                const uint16_t* bias_g = reinterpret_cast<const uint16_t*>(pr.bias);
-                for (int i = lane; i < BN; i += 32) {
-                    const int n = tc.n0 + i;
-                    bias_s[i] = (n < pr.N) ? bias_g[n] : uint16_t(0);   // +0 in both encodings
-                }
-            }
 
             uint32_t ok = 1;
             if (lane == 0) ok = wait_bounded<CG>(tfull_bar(acc), acc_phase, p, abort_addr, ROLE_EPILOGUE, t, 16 + acc) ? 1u : 0u;
@@ -597,7 +559,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             if (tracer) p.trace_tiles[4 * t + 2] = ptx::globaltimer_ns();
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
-            const int CHUNKS = tc.width / Cfg::CW;
+            constexpr int CHUNKS = BN / Cfg::CW;
 #pragma unroll 1
             for (int c = 0; c < CHUNKS; ++c) {
                 float v[Cfg::CW];
@@ -627,13 +589,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 if (!active || n_chunk >= pr.N) continue;
 
                 if (epi != EPI_NONE) {
-                    const uint16_t* bs = bias_s + c * Cfg::CW;
-                    if (pr.flags & FLAG_BIAS_F16) {
+                    // bias[n_chunk .. n_chunk + CW): the same values for every lane (broadcast loads)
+                    const uint16_t* bg = reinterpret_cast<const uint16_t*>(pr.bias) + n_chunk;
+                    const bool f16b = (pr.flags & FLAG_BIAS_F16) != 0;
+                    auto widen = [&](uint32_t h) {
+                        return f16b ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
+                                    : __uint_as_float(h << 16);
+                    };
+                    if (n_chunk + Cfg::CW <= pr.N && (reinterpret_cast<uintptr_t>(bg) & 15u) == 0) {
 #pragma unroll
-                        for (int i = 0; i < Cfg::CW; ++i) v[i] += __half2float(__ushort_as_half(bs[i]));
+                        for (int j = 0; j < Cfg::CW / 8; ++j) {
+                            const uint4 w = __ldg(reinterpret_cast<const uint4*>(bg) + j);
+                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                v[8 * j + 2 * h] += widen(ws[h] & 0xffffu);
+                                v[8 * j + 2 * h + 1] += widen(ws[h] >> 16);
+                            }
+                        }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < Cfg::CW; ++i) v[i] += __uint_as_float(static_cast<uint32_t>(bs[i]) << 16);
+                        for (int i = 0; i < Cfg::CW; ++i) v[i] += (n_chunk + i < pr.N) ? widen(__ldg(bg + i)) : 0.0f;
                     }
                     if (epi == EPI_BIAS_GELU) {
 #pragma unroll

@@ -39,13 +39,6 @@ def tile(request, monkeypatch):
     return request.param
 
 
-@pytest.fixture(params=["split", "nosplit"])
-def split(request, monkeypatch):
-    """Dense launches split a partly filled last wave into half-width tiles unless TG_SPLIT_TAIL=0."""
-    monkeypatch.setenv("TG_SPLIT_TAIL", "1" if request.param == "split" else "0")
-    return request.param
-
-
 @pytest.fixture(autouse=True, scope="module")
 def _built():
     from grouped_gemm_persistent_gb300.build import build
@@ -69,7 +62,7 @@ def test_dense_256_workload():
 @pytest.mark.parametrize("a_col,b_col", LAYOUTS)
 @pytest.mark.parametrize("epi", ["none", "bias", "bias_gelu"])
 @pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
-def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype, tile, split):
+def test_dense_ragged_all_variants(a_col, b_col, epi, c_dtype, tile):
     # spans several tiles with a ragged tail in M, N and K (K not a multiple of 64)
     case = wl.dense_random(333, 392, 200, seed=100, dist="uniform", a_col_major=a_col, b_col_major=b_col,
                            epi=epi, c_dtype=c_dtype, **lds(333, 392, 200, a_col, b_col))
@@ -99,7 +92,7 @@ def test_padded_leading_dimensions():
     assert torch.isnan(c_full[:, 136:].float()).all(), "columns beyond N were written"
 
 
-def test_integer_exact_bitwise(tile, split):
+def test_integer_exact_bitwise(tile):
     # integers in [-4, 4]: every fp32 partial sum is exact, so C must equal the
     # exact result bit for bit (fp32 out) and its RNE rounding (bf16 out)
     for a_col, b_col in LAYOUTS:
@@ -155,7 +148,7 @@ def test_empty_m_or_n_writes_nothing():
     _sync_ok()
 
 
-def test_guard_bands_untouched(tile, split):
+def test_guard_bands_untouched(tile):
     case = wl.dense_random(300, 264, 128, seed=12, dist="normal", epi="bias")
     big = torch.full((300 + 64, 264 + 40), float("inf"), dtype=torch.float32, device="cuda")
     out = big[32:332, 8:272]
@@ -226,7 +219,7 @@ def test_f16_operands(a_col, b_col, epi, out_dtype, tile):
     assert r["ok"] and r["max_tight"] < 4.0, r
 
 
-def test_f16_integer_exact(tile, split):
+def test_f16_integer_exact(tile):
     a, b, _ = _f16_case(300, 264, 640, 62, False, True, ints=True)
     out = tg.gemm(a.cuda(), b.cuda().t(), out_dtype=torch.float32)
     _sync_ok()
