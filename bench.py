@@ -41,6 +41,7 @@ WORKLOADS = {
     "dense_4096_bias_gelu": ["dense_4096_bias_gelu"],
     "dense_8192_f32": ["dense_8192_f32"],
     "grouped_moe": ["grouped_moe"],
+    "grouped_moe_devcounts": ["grouped_moe_devcounts"],
     "skinny_bcast": ["skinny_bcast"],
     "skinny_bcast_ikbo": ["skinny_bcast_ikbo"],
     "dense_256": ["dense_256"],
@@ -178,7 +179,9 @@ class Part:
         self.name = name
         self.grouped = name in wl.GROUPED_WORKLOADS
         self.bcast = name.endswith("_ikbo")          # in-kernel broadcast form of a repeated-row workload
-        base = name[: -len("_ikbo")] if self.bcast else name
+        self.devcounts = name.endswith("_devcounts")  # MoE with the token counts in device memory
+        base = name[: -len("_ikbo")] if self.bcast else (name[: -len("_devcounts")] if self.devcounts else name)
+        self.grouped = self.grouped or self.devcounts
         self.case = wl.grouped_case(base) if self.grouped else wl.dense_case(base)
         self.flops = self.case.flops
         self.bytes = self.case.bcast_bytes if self.bcast else self.case.algorithmic_bytes
@@ -210,6 +213,8 @@ class Part:
         rows = int(c.counts.sum()) if self.grouped else c.M
         self.dev["out"] = torch.empty((rows, c.N), dtype=dt, device="cuda")
         self.host["out"] = torch.empty((rows, c.N), dtype=dt).pin_memory()
+        if self.devcounts:
+            self.dev_counts = torch.tensor(c.counts, dtype=torch.int32, device="cuda")
         if self.grouped:
             import grouped_gemm_persistent_gb300 as tg
             self.table = tg.build_moe_table(self.dev["a"], self.dev["b"], c.counts, self.dev["out"],
@@ -220,7 +225,10 @@ class Part:
     def launch(self, stream):
         import grouped_gemm_persistent_gb300 as tg
         c, d = self.case, self.dev
-        if self.grouped:
+        if self.devcounts:
+            tg.moe_gemm_device(d["a"], d["b"], self.dev_counts, d["out"], bias=d.get("bias"), epilogue=c.epi,
+                               stream=stream)
+        elif self.grouped:
             tg.grouped_gemm_table(self.table, stream)
         elif self.bcast:
             tg.gemm_bcast(d["a"], d["b"], c.repeat, d["out"], bias=d.get("bias"), epilogue=c.epi, stream=stream)

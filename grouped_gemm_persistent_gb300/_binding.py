@@ -74,6 +74,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_gemm_ex.argtypes = [ctypes.POINTER(GroupProblem), vp]
         lib.tg_gemm_bcast.restype = ci
         lib.tg_gemm_bcast.argtypes = [vp, ci, i64, i64, i64, vp, ci, i64, vp, ci, i64, i64, i64, ci, vp, vp]
+        lib.tg_moe_gemm.restype = ci
+        lib.tg_moe_gemm.argtypes = [vp, i64, i64, i64, vp, ci, i64, i64, i64, i64, vp, ci, i64, vp, ci, vp, vp]
         lib.tg_grouped_gemm.restype = ci
         lib.tg_grouped_gemm.argtypes = [ctypes.POINTER(GroupProblem), ci, vp]
         lib.tg_grouped_gemm_noalloc.restype = ci
@@ -198,6 +200,45 @@ def gemm_bcast(a_user: torch.Tensor, b: torch.Tensor, repeat: int, out: torch.Te
     _check(load().tg_gemm_bcast(_ptr(a_user), la, lda, U, repeat, _ptr(b), lb, ldb, _ptr(out),
                                 _DTYPE_CODE[out.dtype], ldc, N, K, epi,
                                 _ptr(bias) if epi else None, _stream_handle(stream)))
+    return out
+
+
+def moe_gemm_device(a: torch.Tensor, b: torch.Tensor, counts: torch.Tensor, out: torch.Tensor | None = None, *,
+                    bias: torch.Tensor | None = None, epilogue: str = "none",
+                    out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """MoE expert GEMM with the token counts on the GPU (tg_moe_gemm): no host round trip.
+
+    ``a`` [T, K] bf16 row-major, rows grouped by expert; ``b`` [G, K, N] bf16 with
+    each expert row-major (``b[g]`` contiguous rows) or column-major (a view of
+    a [G, N, K] tensor); ``counts`` int32 CUDA tensor [G]; ``out`` [T, N]; rows
+    past sum(counts) are not written.  ``bias`` is [G, N] bf16.
+    """
+    if a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise TypeError("a and b must be torch.bfloat16")
+    if counts.dtype != torch.int32 or not counts.is_cuda or counts.dim() != 1 or not counts.is_contiguous():
+        raise TypeError("counts must be a contiguous int32 CUDA tensor [G]")
+    T, K = a.shape
+    G, K2, N = b.shape
+    if K != K2 or counts.shape[0] != G:
+        raise ValueError("shapes: a [T, K], b [G, K, N], counts [G]")
+    la, lda = _matrix(a, "a")
+    if la != ROW_MAJOR:
+        raise ValueError("a must be row-major")
+    if b.stride(2) == 1:
+        lb, ldb = ROW_MAJOR, b.stride(1)
+    elif b.stride(1) == 1:
+        lb, ldb = COL_MAJOR, b.stride(2)
+    else:
+        raise ValueError("each expert of b must be row- or column-major")
+    if out is None:
+        out = torch.empty((T, N), dtype=out_dtype, device=a.device)
+    lc, ldc = _matrix(out, "out")
+    epi = EPILOGUES[epilogue]
+    if epi and (bias is None or bias.dtype != torch.bfloat16 or tuple(bias.shape) != (G, N) or not bias.is_contiguous()):
+        raise ValueError("this epilogue needs a contiguous bf16 bias [G, N]")
+    _check(load().tg_moe_gemm(_ptr(a), lda, T, K, _ptr(b), lb, ldb, b.stride(0), G, N, _ptr(out),
+                              _DTYPE_CODE[out.dtype], ldc, counts.data_ptr(), epi, _ptr(bias) if epi else None,
+                              _stream_handle(stream)))
     return out
 
 

@@ -3,7 +3,7 @@
     python -m grouped_gemm_persistent_gb300.build [--force] [--verbose-ptxas]
 
 Translation units compile in parallel: the host API once, the kernel
-instantiations once per (output dtype, dense/grouped) pair.  The result is
+instantiations once per (output dtype, dense / grouped / MoE) pair.  The result is
 grouped_gemm_persistent_gb300/libtg.so; objects go to
 grouped_gemm_persistent_gb300/_build/.  A rebuild happens only when a source
 or a flag changed (content hash).
@@ -30,8 +30,8 @@ FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", I
                 "--expt-relaxed-constexpr"]
 
 UNITS = [("tg_api", "tg_api.cu", [])] + [
-    (f"tg_inst_f{f}_g{g}", "tg_inst.cu", [f"-DTG_INST_F32={f}", f"-DTG_INST_GROUPED={g}"])
-    for f in (0, 1) for g in (0, 1)
+    (f"tg_inst_f{f}_m{m}", "tg_inst.cu", [f"-DTG_INST_F32={f}", f"-DTG_INST_MODE={m}"])
+    for f in (0, 1) for m in (0, 1, 2)
 ]
 
 

@@ -84,6 +84,7 @@ struct DeviceState {
     tg::ErrorRecord* err = nullptr;
     cudaMemPool_t pool = nullptr;
     int units[128] = {};  // resident work units per kernel variant (0 = not yet queried)
+    int moe_units[16] = {};
 };
 
 std::mutex g_mu;
@@ -245,9 +246,10 @@ struct Variant {
     int bn, cta_group, tile_m, cw, bn_cta;
 };
 
-template <int BN, int CG, bool AMN, bool BMN, bool F32, bool GR>
+template <int BN, int CG, bool AMN, bool BMN, bool F32, int MODE>
 constexpr Variant variant() {
-    using C = Config<BN, CG, AMN, BMN, F32, GR>;
+    using C = Config<BN, CG, AMN, BMN, F32, MODE>;
+    static_assert(C::MOE == (MODE == 2) && C::GROUPED == (MODE == 1), "kernel mode");
     return Variant{&tg::launch<C>, &tg::resident_units<C>, C::BN, C::CTA_GROUP, C::TILE_M, C::CW, C::BN_CTA};
 }
 
@@ -262,6 +264,17 @@ const Variant kVariants[] = {
 constexpr int kTilesPerGroup = 16;
 constexpr int kNumVariants = 4 * kTilesPerGroup;
 static_assert(sizeof(kVariants) / sizeof(kVariants[0]) == kNumVariants, "variant table");
+
+const Variant kMoeVariants[] = {
+    TG_FOR_EACH_MOE_TILE(TG_VARIANT_ENTRY, false)
+    TG_FOR_EACH_MOE_TILE(TG_VARIANT_ENTRY, true)
+};
+static_assert(sizeof(kMoeVariants) / sizeof(kMoeVariants[0]) == 16, "MoE variant table");
+static_assert(TG_MOE_MAX_EXPERTS == tg::MOE_MAX_G, "header and kernel agree on the expert limit");
+
+int moe_variant_index(bool f32, int cta_group, int bn, bool bmn) {
+    return (f32 ? 8 : 0) + (cta_group == 2 ? 4 : 0) + (bn == 256 ? 2 : 0) + (bmn ? 1 : 0);
+}
 
 int variant_index(bool grouped, bool f32, int cta_group, int bn, bool amn, bool bmn) {
     const int tile = (cta_group == 2 ? 8 : 0) + (bn == 256 ? 4 : 0) + (amn ? 2 : 0) + (bmn ? 1 : 0);
@@ -569,6 +582,78 @@ tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
 }
 
+tg_status tg_moe_gemm(const void* A, int64_t lda, int64_t T, int64_t K, const void* B, tg_layout layout_b,
+                      int64_t ldb, int64_t expert_stride, int64_t G, int64_t N, void* C, tg_dtype c_dtype,
+                      int64_t ldc, const int32_t* counts, tg_epilogue epi, const void* bias, tg_stream_t stream) {
+    if (T < 0 || K < 0 || N < 0 || G < 0)
+        return fail(TG_ERR_INVALID_ARG, "negative size T=%lld K=%lld N=%lld G=%lld", (long long)T, (long long)K,
+                    (long long)N, (long long)G);
+    if (T == 0 || N == 0 || G == 0) return TG_OK;
+    if (G > TG_MOE_MAX_EXPERTS)
+        return fail(TG_ERR_UNSUPPORTED, "G=%lld experts; the device-counts form takes at most %d", (long long)G,
+                    TG_MOE_MAX_EXPERTS);
+    if (!counts) return fail(TG_ERR_INVALID_ARG, "counts is NULL");
+    if (reinterpret_cast<uintptr_t>(counts) & 3u) return fail(TG_ERR_INVALID_ARG, "counts is not 4-byte aligned");
+    if (N % 8) return fail(TG_ERR_UNSUPPORTED, "N=%lld must be a multiple of 8 in the device-counts form", (long long)N);
+    const Prob q{A, TG_ROW_MAJOR, lda, B, layout_b, ldb, C, c_dtype, ldc, T, N, K, epi, bias, TG_BF16};
+    tg_status s = check(q, 0);
+    if (s != TG_OK) return s;
+    if (K > 0) {
+        const int64_t min_stride = (layout_b == TG_ROW_MAJOR ? K : N) * ldb;
+        if (expert_stride < min_stride)
+            return fail(TG_ERR_INVALID_ARG, "expert_stride=%lld < %lld (one expert's B)", (long long)expert_stride,
+                        (long long)min_stride);
+        if ((expert_stride * 2) % 16 || expert_stride > (int64_t(1) << 38))
+            return fail(TG_ERR_UNSUPPORTED, "expert_stride must be a multiple of 8 elements below 2^38 (TMA)");
+    }
+    DeviceState* d = nullptr;
+    if ((s = device_state(&d)) != TG_OK) return s;
+    if ((s = encoder()) != TG_OK) return s;
+
+    const TileChoice tc = pick_tile(T, N, d->sms);
+    const int vi = moe_variant_index(c_dtype == TG_F32, tc.cta_group, tc.bn, layout_b == TG_ROW_MAJOR);
+    const Variant& v = kMoeVariants[vi];
+    int units = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        units = d->moe_units[vi];
+    }
+    if (units <= 0) {
+        cudaError_t e = v.units(&units);
+        if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+        if (units <= 0) return fail(TG_ERR_UNSUPPORTED, "MoE kernel variant %d cannot be resident", vi);
+        std::lock_guard<std::mutex> lock(g_mu);
+        d->moe_units[vi] = units;
+    }
+
+    Params p;
+    std::memset(&p, 0, sizeof p);
+    if ((s = fill_problem(q, v, 0, &p.dense)) != TG_OK) return s;
+    if (K > 0) {
+        // B as one 3-D tensor: expert g is the outermost coordinate
+        if (layout_b == TG_ROW_MAJOR)
+            s = make_map_3d(&p.dense.tma_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, G, ldb * 2, expert_stride * 2,
+                            64, 64, 1, "B (experts)");
+        else
+            s = make_map_3d(&p.dense.tma_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, G, ldb * 2, expert_stride * 2,
+                            64, v.bn_cta, 1, "B (experts)");
+        if (s != TG_OK) return s;
+    }
+    p.num_problems = 1;
+    p.total_tiles = 0;   // the kernel derives it from the device counts
+    p.band = pick_band(p.dense.tiles_n, units);
+    p.moe_counts = counts;
+    p.moe_groups = static_cast<int32_t>(G);
+    p.moe_rows = T;
+    p.moe_c = C;
+    p.moe_ldc = ldc;
+    base_params(&p, d);
+    const int grid = units * v.cta_group;
+    cudaError_t e = v.launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return TG_OK;
+}
+
 tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stream) {
     if (G < 0 || G > 65536) return fail(TG_ERR_INVALID_ARG, "G=%d out of range [0, 65536]", G);
     if (G == 0) return TG_OK;
@@ -763,6 +848,10 @@ tg_status tg_device_status(tg_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "clearing the device error record");
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "clearing the device error record");
+    if (rec.code == tg::ERR_COUNTS)
+        return fail(TG_ERR_INVALID_ARG,
+                    "device token counts are negative or sum to %lld rows, more than T; the launch computed nothing",
+                    (long long)rec.tile);
     static const char* roles[] = {"?", "TMA producer", "MMA issuer", "epilogue", "MMA drain"};
     return fail(TG_ERR_TIMEOUT, "in-kernel wait ran out: role=%s block=%u stage=%u tile=%lld waited=%.1f ms",
                 rec.role < 5 ? roles[rec.role] : "?", rec.block, rec.stage, (long long)rec.tile,

@@ -1,12 +1,12 @@
 // tg_inst.cu - explicit instantiations of the GEMM kernel and its launcher.
-// Compiled once per (TG_INST_F32, TG_INST_GROUPED) pair.
+// Compiled once per (TG_INST_F32, TG_INST_MODE) pair; MODE 0 dense, 1 grouped, 2 MoE.
 #include "tg_launch.cuh"
 
 #ifndef TG_INST_F32
 #error "define TG_INST_F32 (0/1)"
 #endif
-#ifndef TG_INST_GROUPED
-#error "define TG_INST_GROUPED (0/1)"
+#ifndef TG_INST_MODE
+#error "define TG_INST_MODE (0/1/2)"
 #endif
 
 namespace tg {
@@ -63,10 +63,14 @@ cudaError_t resident_units(int* units) {
     return cudaOccupancyMaxActiveClusters(units, kern, &cfg);
 }
 
-#define TG_INSTANTIATE(BN, CG, AMN, BMN, F32, GR)                                                        \
-    template cudaError_t launch<Config<BN, CG, AMN, BMN, F32, GR>>(const Params&, int, cudaStream_t);   \
-    template cudaError_t resident_units<Config<BN, CG, AMN, BMN, F32, GR>>(int*);
+#define TG_INSTANTIATE(BN, CG, AMN, BMN, F32, MODE)                                                        \
+    template cudaError_t launch<Config<BN, CG, AMN, BMN, F32, MODE>>(const Params&, int, cudaStream_t);   \
+    template cudaError_t resident_units<Config<BN, CG, AMN, BMN, F32, MODE>>(int*);
 
-TG_FOR_EACH_TILE(TG_INSTANTIATE, (TG_INST_F32 != 0), (TG_INST_GROUPED != 0))
+#if TG_INST_MODE == 2
+TG_FOR_EACH_MOE_TILE(TG_INSTANTIATE, (TG_INST_F32 != 0))
+#else
+TG_FOR_EACH_TILE(TG_INSTANTIATE, (TG_INST_F32 != 0), TG_INST_MODE)
+#endif
 
 }  // namespace tg

@@ -51,8 +51,9 @@ constexpr int EPI_WARP0 = 2;         // warps 2..5 drain TMEM; warp w reads lane
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int C_STAGE_BYTES = 32 * 128;   // per-warp store staging buffer: 32 rows x 128 bytes
 constexpr int SMEM_LIMIT = 232448;        // max dynamic shared memory per CTA on sm_100 family
+constexpr int MOE_MAX_G = 190;            // experts per call of the device-counts MoE form (table in shared memory)
 
-enum : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1 };
+enum : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_COUNTS = 2 };
 enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4 };
 enum : int32_t { EPI_NONE = 0, EPI_BIAS = 1, EPI_BIAS_GELU = 2 };
 
@@ -108,16 +109,26 @@ struct Params {
     int64_t trace_tiles_cap;
     uint64_t* trace_ctas;
     int64_t trace_ctas_cap;
+    // Device-counts MoE form: expert g owns rows [off_g, off_g + moe_counts[g]) of A and C,
+    // off_g = sum of the counts before g; B is a 3-D map [G][K][N] (or [G][N][K]).
+    const int32_t* moe_counts;
+    int32_t moe_groups;
+    int64_t moe_rows;           // T: rows of A and C; the counts must sum to at most T
+    void* moe_c;                // C base pointer, for rows stored without TMA
+    int64_t moe_ldc;            // elements per row of C
 };
 
-template <int BN_, int CTA_GROUP_, bool A_MN_, bool B_MN_, bool C_F32_, bool GROUPED_>
+// MODE: 0 dense (tensor maps in parameter space), 1 grouped (problem table in
+// device memory), 2 MoE with device-resident token counts.
+template <int BN_, int CTA_GROUP_, bool A_MN_, bool B_MN_, bool C_F32_, int MODE_>
 struct Config {
     static constexpr int BN = BN_;                   // tile columns (whole pair)
     static constexpr int CTA_GROUP = CTA_GROUP_;
     static constexpr bool A_MN = A_MN_;              // A stored M-contiguous (column-major)
     static constexpr bool B_MN = B_MN_;              // B stored N-contiguous (row-major K x N)
     static constexpr bool C_F32 = C_F32_;
-    static constexpr bool GROUPED = GROUPED_;
+    static constexpr bool GROUPED = MODE_ == 1;
+    static constexpr bool MOE = MODE_ == 2;
     static constexpr int BN_CTA = BN / CTA_GROUP;    // B columns each CTA loads
     static constexpr int TILE_M = BM * CTA_GROUP;    // rows per tile (pair)
     static constexpr int A_BYTES = BM * BK * 2;
@@ -126,19 +137,22 @@ struct Config {
     static constexpr int CW = C_F32 ? 32 : 64;       // output columns per 128-byte staged row
     static constexpr int TMEM_COLS = 2 * BN;         // two fp32 accumulators of BN columns
     static constexpr int C_BYTES = NUM_EPI_WARPS * 2 * C_STAGE_BYTES;
-    static constexpr int FIXED = C_BYTES + 512 /*barriers and slots*/ + 1024 /*alignment slack*/;
+    static constexpr int MOE_BYTES = MOE ? 8 * (MOE_MAX_G + 1) : 0;   // tile and row prefix sums
+    static constexpr int FIXED = C_BYTES + MOE_BYTES + 512 /*barriers and slots*/ + 1024 /*alignment slack*/;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_BAR = OFF_C + C_BYTES;
+    static constexpr int OFF_MOE = OFF_C + C_BYTES;
+    static constexpr int OFF_BAR = OFF_MOE + MOE_BYTES;
     // barriers: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
-    static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+    static constexpr int OFF_MOE_TOTAL = OFF_ABORT + 4;
+    static constexpr int SMEM_BYTES = OFF_MOE_TOTAL + 4 + 1024;
 
 
     static_assert(BN == 128 || BN == 256, "tile width");
@@ -154,10 +168,18 @@ struct Config {
 // scheduling helpers
 
 struct TileCoord {
-    int g;        // problem index
-    int m0;       // first accumulator row of this CTA
+    int g;        // problem (grouped) or expert (MoE) index
+    int m0;       // first accumulator row of this CTA (MoE: a row of the whole A / C)
     int n0;       // first column of the tile
     int r;        // replica index (broadcast form), else 0
+    int row_end;  // MoE: first row past this expert's rows; otherwise INT32_MAX
+};
+
+// Device-counts MoE schedule, built in shared memory by every CTA at start:
+// tile_pref[g] = tiles of experts before g, row_off[g] = rows before g.
+struct MoeTable {
+    const int32_t* tile_pref;   // [G + 1]
+    const int32_t* row_off;     // [G + 1]
 };
 
 template <class Cfg>
@@ -166,11 +188,14 @@ __device__ __forceinline__ const Problem& problem_of(const Params& p, int g) {
     else return p.dense;
 }
 
-// Problem containing global tile t; `g` is a hint that only moves forward.
+// Problem (or expert) containing global tile t; `g` is a hint that only moves forward.
 template <class Cfg>
-__device__ __forceinline__ int find_problem(const Params& p, int64_t t, int g) {
+__device__ __forceinline__ int find_problem(const Params& p, int64_t t, int g, const MoeTable& mt = {}) {
     if constexpr (Cfg::GROUPED) {
         while (g + 1 < p.num_problems && p.problems[g + 1].tile_begin <= t) ++g;
+        return g;
+    } else if constexpr (Cfg::MOE) {
+        while (g + 1 < p.moe_groups && mt.tile_pref[g + 1] <= t) ++g;
         return g;
     } else {
         return 0;
@@ -178,16 +203,22 @@ __device__ __forceinline__ int find_problem(const Params& p, int64_t t, int g) {
 }
 
 template <class Cfg>
-__device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int g, uint32_t rank) {
+__device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int g, uint32_t rank,
+                                                const MoeTable& mt = {}) {
     const Problem& pr = problem_of<Cfg>(p, g);
     int64_t local = t - pr.tile_begin;
+    int tiles_m = pr.tiles_m;
+    if constexpr (Cfg::MOE) {
+        local = t - mt.tile_pref[g];
+        tiles_m = (mt.tile_pref[g + 1] - mt.tile_pref[g]) / pr.tiles_n;
+    }
     int replica = 0;
     if (pr.replicas > 1) {   // replicas of one tile are adjacent: they share A and B in L2
         replica = static_cast<int>(local % pr.replicas);
         local /= pr.replicas;
     }
     const int band = p.band;
-    const int64_t per_band = static_cast<int64_t>(pr.tiles_m) * band;
+    const int64_t per_band = static_cast<int64_t>(tiles_m) * band;
     const int b = static_cast<int>(local / per_band);
     const int r = static_cast<int>(local - static_cast<int64_t>(b) * per_band);
     const int n_first = b * band;
@@ -199,6 +230,11 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     c.m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
     c.n0 = nb * Cfg::BN;
     c.r = replica;
+    c.row_end = INT32_MAX;
+    if constexpr (Cfg::MOE) {
+        c.m0 += mt.row_off[g];
+        c.row_end = mt.row_off[g + 1];
+    }
     return c;
 }
 
@@ -352,6 +388,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         ptx::tmem_alloc<CG>(tmem_slot, Cfg::TMEM_COLS);
         ptx::tmem_relinquish<CG>();
     }
+    if constexpr (Cfg::MOE) {
+        if (warp == EPI_WARP0) {
+            // Prefix sums of the device-resident token counts: rows and tiles before each expert.
+            int32_t* tile_pref = reinterpret_cast<int32_t*>(smem + Cfg::OFF_MOE);
+            int32_t* row_off = tile_pref + (MOE_MAX_G + 1);
+            const int G = p.moe_groups;
+            const int64_t tiles_n = p.dense.tiles_n;
+            long long rows = 0, tiles = 0;
+            bool bad = false;
+            if (lane == 0) { tile_pref[0] = 0; row_off[0] = 0; }
+            for (int base = 0; base < G; base += 32) {
+                const int i = base + lane;
+                long long c = (i < G) ? static_cast<long long>(__ldg(p.moe_counts + i)) : 0ll;
+                bad |= c < 0;
+                c = c < 0 ? 0 : c;
+                long long tl = (c + Cfg::TILE_M - 1) / Cfg::TILE_M * tiles_n;
+                for (int d = 1; d < 32; d <<= 1) {   // inclusive warp scan
+                    const long long xc = __shfl_up_sync(0xffffffffu, c, d);
+                    const long long xt = __shfl_up_sync(0xffffffffu, tl, d);
+                    if (lane >= d) { c += xc; tl += xt; }
+                }
+                if (i < G) {
+                    row_off[i + 1] = static_cast<int32_t>(min(rows + c, 0x7fffffffll));
+                    tile_pref[i + 1] = static_cast<int32_t>(min(tiles + tl, 0x7fffffffll));
+                }
+                rows += __shfl_sync(0xffffffffu, c, 31);
+                tiles += __shfl_sync(0xffffffffu, tl, 31);
+            }
+            bad = __any_sync(0xffffffffu, bad) || rows > p.moe_rows;
+            if (lane == 0) {
+                *reinterpret_cast<volatile int32_t*>(smem + Cfg::OFF_MOE_TOTAL) = bad ? 0 : static_cast<int32_t>(tiles);
+                if (bad && blockIdx.x == 0 && atomicCAS(&p.err->code, ERR_NONE, ERR_COUNTS) == ERR_NONE) {
+                    p.err->role = 0;
+                    p.err->block = 0;
+                    p.err->stage = 0;
+                    p.err->tile = rows;
+                    p.err->waited_ns = 0;
+                }
+            }
+        }
+    }
     if constexpr (!Cfg::GROUPED) {
         if (threadIdx.x == 0) {
             ptx::prefetch_tensormap(&p.dense.tma_a);
@@ -363,6 +440,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_TMEM_SLOT);
+    int64_t total_tiles = p.total_tiles;
+    MoeTable mt{};
+    if constexpr (Cfg::MOE) {
+        total_tiles = *reinterpret_cast<volatile int32_t*>(smem + Cfg::OFF_MOE_TOTAL);
+        mt.tile_pref = reinterpret_cast<const int32_t*>(smem + Cfg::OFF_MOE);
+        mt.row_off = mt.tile_pref + (MOE_MAX_G + 1);
+    }
     if (p.trace_ctas && threadIdx.x == 0 && blockIdx.x < p.trace_ctas_cap)
         p.trace_ctas[2 * blockIdx.x] = ptx::globaltimer_ns();
 
@@ -375,8 +459,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             int64_t issued = 0;          // k-blocks whose loads this thread issued
             bool aborted = false;
             bool withhold = (p.withhold_kb >= 0) && blockIdx.x == 0;
-            for (int64_t t = unit; t < p.total_tiles && !aborted; t += num_units) {
-                g = find_problem<Cfg>(p, t, g);
+            for (int64_t t = unit; t < total_tiles && !aborted; t += num_units) {
+                g = find_problem<Cfg>(p, t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 if constexpr (Cfg::GROUPED) {
                     if (g != g_fenced) {
@@ -385,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         g_fenced = g;
                     }
                 }
-                const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
+                const TileCoord tc = tile_coord<Cfg>(p, t, g, rank, mt);
                 const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // first B column this CTA loads
                 for (int kb = 0; kb < pr.k_blocks; ++kb) {
                     if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, t, stage)) {
@@ -409,7 +493,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         } else {
                             load(a_dst, &pr.tma_a, k0, tc.m0);
                         }
-                        if constexpr (Cfg::B_MN) {
+                        if constexpr (Cfg::MOE) {
+                            auto load3 = [&](uint32_t dst, int x, int y) {
+                                if constexpr (CG == 2) ptx::tma_load_3d_pair(dst, &pr.tma_b, x, y, tc.g, fb);
+                                else ptx::tma_load_3d(dst, &pr.tma_b, x, y, tc.g, fb);
+                            };
+                            if constexpr (Cfg::B_MN) {
+#pragma unroll
+                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load3(b_dst + j * 8192, nb0 + j * 64, k0);
+                            } else {
+                                load3(b_dst, k0, nb0);
+                            }
+                        } else if constexpr (Cfg::B_MN) {
 #pragma unroll
                             for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
                         } else {
@@ -460,8 +555,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 if (lane == 0) ok = wait_bounded<CG, false>(bar, par, p, abort_addr, ROLE_MMA, tile, st) ? 1u : 0u;
                 return __shfl_sync(0xffffffffu, ok, 0) != 0;
             };
-            for (int64_t t = unit; t < p.total_tiles && !aborted; t += num_units) {
-                g = find_problem<Cfg>(p, t, g);
+            for (int64_t t = unit; t < total_tiles && !aborted; t += num_units) {
+                g = find_problem<Cfg>(p, t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 const uint32_t idesc = pr.idesc;
                 if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, t, 16 + acc)) {
@@ -534,8 +629,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         uint32_t acc_phase = 0;
         int sbuf = 0;
         int g = 0, g_fenced = -1;
-        for (int64_t t = unit; t < p.total_tiles; t += num_units) {
-            g = find_problem<Cfg>(p, t, g);
+        for (int64_t t = unit; t < total_tiles; t += num_units) {
+            g = find_problem<Cfg>(p, t, g, mt);
             const Problem& pr = problem_of<Cfg>(p, g);
             if constexpr (Cfg::GROUPED) {
                 if (lane == 0 && g != g_fenced) {
@@ -543,9 +638,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     g_fenced = g;
                 }
             }
-            const TileCoord tc = tile_coord<Cfg>(p, t, g, rank);
+            const TileCoord tc = tile_coord<Cfg>(p, t, g, rank, mt);
             const int row0 = tc.m0 + q * 32;
-            const bool active = row0 < pr.M;
+            int row_limit = pr.M;                     // rows of C this tile may write: [.., row_limit)
+            if constexpr (Cfg::MOE) row_limit = static_cast<int>(min(static_cast<int64_t>(tc.row_end), p.moe_rows));
+            const bool active = row0 < row_limit;
+            // MoE: a slab that runs past its expert's rows is written row by row, without TMA
+            const bool direct = Cfg::MOE && row0 + 32 > row_limit;
             const int epi = pr.epi;
 
 
@@ -590,7 +689,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
                 if (epi != EPI_NONE) {
                     // bias[n_chunk .. n_chunk + CW): the same values for every lane (broadcast loads)
-                    const uint16_t* bg = reinterpret_cast<const uint16_t*>(pr.bias) + n_chunk;
+                    const uint16_t* bg = reinterpret_cast<const uint16_t*>(pr.bias) + n_chunk +
+                                         (Cfg::MOE ? static_cast<int64_t>(tc.g) * pr.N : 0);
                     const bool f16b = (pr.flags & FLAG_BIAS_F16) != 0;
                     auto widen = [&](uint32_t h) {
                         return f16b ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
@@ -619,10 +719,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
                 // stage: this lane's row (128 bytes) as eight 16-byte chunks, 128-byte swizzled
                 const uint32_t buf = c_stage0 + sbuf * C_STAGE_BYTES;
-                if (lane == 0) ptx::bulk_wait_group_read<1>();
-                __syncwarp();
+                if (!direct) {
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
+                }
                 const uint32_t row_addr = buf + lane * 128;
                 const bool c_f16 = (pr.flags & FLAG_C_F16) != 0;
+                constexpr int ESIZE = Cfg::C_F32 ? 4 : 2;
+                uint8_t* row_ptr = nullptr;           // direct stores: this lane's row of C
+                if constexpr (Cfg::MOE) {
+                    if (direct && row0 + lane < row_limit)
+                        row_ptr = static_cast<uint8_t*>(p.moe_c) +
+                                  (static_cast<int64_t>(row0 + lane) * p.moe_ldc + n_chunk) * ESIZE;
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint32_t w0, w1, w2, w3;
@@ -642,10 +751,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         w2 = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
                         w3 = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
                     }
+                    if (direct) {
+                        // 16 bytes = 16 / ESIZE columns; N is a multiple of 8 on this path
+                        if (row_ptr && n_chunk + (j + 1) * (16 / ESIZE) <= pr.N)
+                            *reinterpret_cast<uint4*>(row_ptr + 16 * j) = make_uint4(w0, w1, w2, w3);
+                        continue;
+                    }
                     const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                  :: "r"(dst), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
                 }
+                if (direct) continue;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {

@@ -21,7 +21,8 @@ cudaError_t resident_units(int* units);
 
 }  // namespace tg
 
-// Every (BN, CTA_GROUP, A_MN, B_MN) combination for one (C_F32, GROUPED) pair.
+// Every (BN, CTA_GROUP, A_MN, B_MN) combination for one (C_F32, MODE) pair
+// (MODE 0 dense, 1 grouped table; the argument named GROUPED is that MODE).
 // Index within the list: (CTA_GROUP == 2) * 8 + (BN == 256) * 4 + A_MN * 2 + B_MN.
 #define TG_FOR_EACH_TILE(X, C_F32, GROUPED)          \
     X(128, 1, false, false, C_F32, GROUPED)          \
@@ -40,3 +41,15 @@ cudaError_t resident_units(int* units);
     X(256, 2, false, true, C_F32, GROUPED)           \
     X(256, 2, true, false, C_F32, GROUPED)           \
     X(256, 2, true, true, C_F32, GROUPED)
+
+// The device-counts MoE form (MODE 2): A is always row-major [T, K].
+// Index within the list: (CTA_GROUP == 2) * 4 + (BN == 256) * 2 + B_MN.
+#define TG_FOR_EACH_MOE_TILE(X, C_F32)   \
+    X(128, 1, false, false, C_F32, 2)     \
+    X(128, 1, false, true, C_F32, 2)      \
+    X(256, 1, false, false, C_F32, 2)     \
+    X(256, 1, false, true, C_F32, 2)      \
+    X(128, 2, false, false, C_F32, 2)     \
+    X(128, 2, false, true, C_F32, 2)      \
+    X(256, 2, false, false, C_F32, 2)     \
+    X(256, 2, false, true, C_F32, 2)

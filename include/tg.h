@@ -162,6 +162,38 @@ tg_status tg_gemm_ex(const tg_group_problem *problem, tg_stream_t stream);
  */
 tg_status tg_grouped_gemm(const tg_group_problem *table, int G, tg_stream_t stream);
 
+/* Largest number of experts tg_moe_gemm accepts (its schedule lives in shared memory). */
+#define TG_MOE_MAX_EXPERTS 190
+
+/*
+ * tg_moe_gemm - MoE expert GEMM whose per-expert token counts are in DEVICE
+ * memory, as a router running on the GPU produces them: one launch, no
+ * host round trip and no per-expert descriptors (the MoE layer of the TLX
+ * article's third case study, with counts that never leave the GPU).
+ *
+ *   A, lda, T, K     : bf16 [T, K] row-major; expert g owns rows
+ *                      [off_g, off_g + counts[g]), off_g = counts[0] + ... + counts[g-1].
+ *   B, layout_b, ldb, expert_stride, G, N :
+ *                      bf16 experts; expert g's K x N matrix starts at
+ *                      B + g * expert_stride (elements) and is row-major
+ *                      (ldb >= N) or column-major (ldb >= K).
+ *   C, c_dtype, ldc  : [T, N] row-major, same row grouping as A.
+ *   counts           : DEVICE int32[G], read by the kernel.  Rows past the sum
+ *                      of the counts are not written.
+ *   epi, bias        : bias is bf16 [G, N] (row g for expert g).
+ *
+ * Limits: G <= TG_MOE_MAX_EXPERTS; N a multiple of 8; TMA alignment rules as
+ * for tg_gemm; expert_stride a multiple of 8 elements.  Counts that are
+ * negative or sum to more than T make the launch compute nothing and
+ * tg_device_status report TG_ERR_INVALID_ARG.  Results are bitwise equal to
+ * tg_grouped_gemm on the same rows.
+ */
+tg_status tg_moe_gemm(const void *A, int64_t lda, int64_t T, int64_t K,
+                      const void *B, tg_layout layout_b, int64_t ldb, int64_t expert_stride, int64_t G, int64_t N,
+                      void *C, tg_dtype c_dtype, int64_t ldc,
+                      const int32_t *counts, tg_epilogue epi, const void *bias,
+                      tg_stream_t stream);
+
 /*
  * Largest number of non-empty problems tg_grouped_gemm_noalloc accepts in one
  * call: the size of its fixed device-side problem table.
@@ -204,7 +236,8 @@ const char *tg_last_error_message(void);
 /*
  * tg_device_status - synchronise `stream`, then read and clear the current
  * device's error record.  Returns TG_OK, TG_ERR_CUDA (the stream reported a
- * CUDA error), or TG_ERR_TIMEOUT (a kernel's bounded mbarrier wait ran out:
+ * CUDA error), TG_ERR_INVALID_ARG (tg_moe_gemm found invalid device counts),
+ * or TG_ERR_TIMEOUT (a kernel's bounded mbarrier wait ran out:
  * the kernel recorded the role, tile and stage, stopped, drained its own
  * in-flight copies and MMAs, freed its tensor memory and returned; the context
  * stays usable).  The record is per device and shared by all streams.

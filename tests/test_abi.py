@@ -164,3 +164,15 @@ def test_bcast_argument_checks(lib):
     assert bc(C=None) == tg.TG_ERR_INVALID_ARG
     assert bc(lda=32) == tg.TG_ERR_INVALID_ARG
     assert bc(U=0) == tg.TG_OK
+
+
+def test_moe_argument_checks(lib):
+    def moe(T=256, K=64, G=4, N=64, counts=0x40000, A=ALIGNED, B=ALIGNED_B, C=ALIGNED_C, stride=64 * 64, lb=0):
+        return lib.tg_moe_gemm(A, 64, T, K, B, lb, 64, stride, G, N, C, 0, 64, counts, 0, None, None)
+    assert moe(T=0) == tg.TG_OK and moe(G=0) == tg.TG_OK            # nothing to do
+    assert moe(G=191) == tg.TG_ERR_UNSUPPORTED                          # schedule table limit
+    assert moe(counts=None) == tg.TG_ERR_INVALID_ARG
+    assert moe(counts=0x40002) == tg.TG_ERR_INVALID_ARG                 # counts must be 4-byte aligned
+    assert moe(N=60) == tg.TG_ERR_UNSUPPORTED                           # N % 8
+    assert moe(stride=64 * 63) == tg.TG_ERR_INVALID_ARG                 # one expert does not fit its stride
+    assert moe(T=-1) == tg.TG_ERR_INVALID_ARG

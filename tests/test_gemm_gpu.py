@@ -363,6 +363,74 @@ def test_grouped_mixed_layouts_and_dtypes(tile):
         assert r["ok"] and r["max_tight"] < 4.0, r
 
 
+# ------------------------------------------------------------------------------------------ MoE, device counts
+
+def _moe_case(counts, N, K, seed, epi="none", b_col=False, extra_rows=0):
+    case = wl.grouped_random(counts, N, K, seed, epi=epi)
+    T = int(np.sum(counts)) + extra_rows
+    a = torch.zeros((T, K), dtype=torch.bfloat16)
+    a[: case.a.shape[0]] = case.a
+    a = a.cuda()
+    bst = case.b if not b_col else case.b.transpose(1, 2).contiguous()
+    b = bst.cuda()
+    bview = b.transpose(1, 2) if b_col else b
+    bias = case.bias.cuda() if case.bias is not None else None
+    return case, a, bview, bias, T
+
+
+@pytest.mark.parametrize("epi", ["none", "bias_gelu"])
+@pytest.mark.parametrize("b_col", [False, True])
+@pytest.mark.parametrize("c_dtype", [torch.bfloat16, torch.float32])
+def test_moe_device_counts_equal_grouped_bitwise(epi, b_col, c_dtype, tile):
+    counts = [0, 300, 5, 0, 130, 257, 1, 0, 64]
+    case, a, b, bias, T = _moe_case(counts, 136, 200, 51, epi=epi, b_col=b_col)
+    dev = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    out_dev = torch.full((T, 136), float("nan"), dtype=c_dtype, device="cuda")
+    tg.moe_gemm_device(a, b, dev, out_dev, bias=bias, epilogue=epi)
+    out_tab = torch.empty_like(out_dev)
+    tg.moe_grouped_gemm(a, b, counts, out_tab, bias=bias, epilogue=epi)
+    _sync_ok()
+    assert torch.equal(out_dev.view(torch.int16 if c_dtype != torch.float32 else torch.int32),
+                       out_tab.view(torch.int16 if c_dtype != torch.float32 else torch.int32))
+    _check_grouped(case, out_dev, b_col=b_col)
+
+
+def test_moe_rows_past_the_counts_are_untouched(tile):
+    counts = [129, 0, 70]
+    case, a, b, bias, T = _moe_case(counts, 264, 128, 52, extra_rows=77)
+    dev = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    out = torch.full((T, 264), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tg.moe_gemm_device(a, b, dev, out)
+    _sync_ok()
+    used = int(sum(counts))
+    assert not torch.isnan(out[:used].float()).any()
+    assert torch.isnan(out[used:].float()).all(), "rows past sum(counts) were written"
+    _check_grouped(case, out[:used])
+
+
+def test_moe_invalid_device_counts_are_reported():
+    counts_ok = [100, 50]
+    case, a, b, bias, T = _moe_case(counts_ok, 136, 64, 53)
+    out = torch.zeros((T, 136), dtype=torch.bfloat16, device="cuda")
+    for bad in ([100, -1], [100, 51]):            # negative; sum above T
+        tg.moe_gemm_device(a, b, torch.tensor(bad, dtype=torch.int32, device="cuda"), out)
+        with pytest.raises(tg.TGError) as ei:
+            tg.device_status()
+        assert ei.value.status == tg.TG_ERR_INVALID_ARG
+    tg.moe_gemm_device(a, b, torch.tensor(counts_ok, dtype=torch.int32, device="cuda"), out)
+    _sync_ok()
+    _check_grouped(case, out)
+
+
+def test_workload_grouped_moe_device_counts_bitwise():
+    case = wl.grouped_case("grouped_moe")
+    a, b = case.a.cuda(), case.b.cuda()
+    out_dev = tg.moe_gemm_device(a, b, torch.tensor(case.counts, dtype=torch.int32, device="cuda"))
+    out_tab = tg.moe_grouped_gemm(a, b, case.counts)
+    _sync_ok()
+    assert torch.equal(out_dev.view(torch.int16), out_tab.view(torch.int16))
+
+
 # ------------------------------------------------------------------------------------------ failure path
 
 def test_bounded_wait_reports_timeout_and_context_survives(tile):
