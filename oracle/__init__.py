@@ -56,6 +56,9 @@ class Oracle:
         lib.oracle_gemm.restype = ctypes.c_int
         lib.oracle_gemm.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64,
                                     vp, ctypes.c_int, ctypes.c_int, i64, i64, i64, vp, i64, dp, dp]
+        lib.oracle_gemm_norm.restype = ctypes.c_int
+        lib.oracle_gemm_norm.argtypes = [vp, ctypes.c_int, i64, vp, ctypes.c_int, i64, vp, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, ctypes.c_double, i64, i64, i64, vp, i64, dp, dp]
         lib.oracle_f16_to_double.restype = ctypes.c_double
         lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_bf16_to_double.restype = ctypes.c_double
@@ -67,8 +70,8 @@ class Oracle:
         self.path = path
 
     def gemm(self, a, b, *, a_col_major=False, b_col_major=False, bias=None, epi="none", rows=None,
-             in_dtype="bf16"):
-        return _gemm(self.lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype)
+             in_dtype="bf16", row_norm_eps=None):
+        return _gemm(self.lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype, row_norm_eps)
 
     def gelu_tanh(self, z: float) -> float:
         return self.lib.oracle_gelu_tanh(z)
@@ -111,7 +114,8 @@ def _storage(x: np.ndarray, name: str):
 
 
 def gemm(a: np.ndarray, b: np.ndarray, *, a_col_major: bool = False, b_col_major: bool = False,
-         bias: np.ndarray | None = None, epi: str = "none", rows=None, in_dtype: str = "bf16"):
+         bias: np.ndarray | None = None, epi: str = "none", rows=None, in_dtype: str = "bf16",
+         row_norm_eps: float | None = None):
     """Reference y and s for C = epi(A . B).
 
     ``a`` is A's storage: [M, K] (row-major) or [K, M] (column-major, i.e.
@@ -120,15 +124,16 @@ def gemm(a: np.ndarray, b: np.ndarray, *, a_col_major: bool = False, b_col_major
     larger than the row (a padded leading dimension) is allowed.  ``bias`` is
     uint16 [N].  ``rows`` selects output rows (default: all).  ``in_dtype``
     ("bf16" or "f16") is the element type the bit patterns of a, b and bias hold.
-    Returns (y, s), float64 arrays [len(rows), N].
+    ``row_norm_eps`` (a float) first replaces A by rmsnorm(A) with that eps.
+    Returns (y, s), float64 arrays [len(rows), N] (s on the normalised A).
     """
-    return _gemm(default().lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype)
+    return _gemm(default().lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype, row_norm_eps)
 
 
 IN_DTYPES = {"bf16": 0, "f16": 1}
 
 
-def _gemm(lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype="bf16"):
+def _gemm(lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype="bf16", row_norm_eps=None):
     pa, lda = _storage(a, "a")
     pb, ldb = _storage(b, "b")
     M, K = (a.shape[1], a.shape[0]) if a_col_major else a.shape
@@ -149,8 +154,8 @@ def _gemm(lib, a, b, a_col_major, b_col_major, bias, epi, rows, in_dtype="bf16")
         prow, nrow = keep.ctypes.data, keep.shape[0]
     y = np.empty((nrow, N), dtype=np.float64)
     s = np.empty((nrow, N), dtype=np.float64)
-    rc = lib.oracle_gemm(pa, int(a_col_major), lda, pb, int(b_col_major), ldb, pbias, e, IN_DTYPES[in_dtype],
-                         M, N, K, prow, nrow,
+    rc = lib.oracle_gemm_norm(pa, int(a_col_major), lda, pb, int(b_col_major), ldb, pbias, e, IN_DTYPES[in_dtype],
+                              int(row_norm_eps is not None), float(row_norm_eps or 0.0), M, N, K, prow, nrow,
                          y.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
                          s.ctypes.data_as(ctypes.POINTER(ctypes.c_double)))
     if rc != 0:

@@ -31,6 +31,12 @@
  * (Hendrycks & Gimpel, "Gaussian Error Linear Units"), in double with the C
  * library's tanh.
  *
+ * Row normalisation (optional, the "fuse the norm into the GEMM" idea of the
+ * TLX pages): with row_norm set, A is first replaced by rmsnorm(A),
+ *     a'_ik = a_ik / sqrt((1/K) sum_k a_ik^2 + eps),
+ * in double, and the product, bias and GELU follow on a'.  (A gain vector
+ * gamma folds into B: rmsnorm_gamma(A) . B = rmsnorm(A) . diag(gamma) B.)
+ *
  * Element types: A, B and bias are all bf16 or all IEEE binary16 (fp16, the
  * TLX listing's type); both widen exactly to double.
  *
@@ -106,12 +112,13 @@ int oracle_num_threads(void)
  * Returns 0 on success, -1 on a bad argument, -2 when scratch memory for the
  * widened operands cannot be had.
  */
-int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
-                const uint16_t *B, int b_col_major, int64_t ldb,
-                const uint16_t *bias, int epi, int in_dtype,
-                int64_t M, int64_t N, int64_t K,
-                const int64_t *rows, int64_t n_rows,
-                double *Y, double *S)
+int oracle_gemm_norm(const uint16_t *A, int a_col_major, int64_t lda,
+                     const uint16_t *B, int b_col_major, int64_t ldb,
+                     const uint16_t *bias, int epi, int in_dtype,
+                     int row_norm, double eps,
+                     int64_t M, int64_t N, int64_t K,
+                     const int64_t *rows, int64_t n_rows,
+                     double *Y, double *S)
 {
     if (M < 0 || N < 0 || K < 0 || !Y || !S) return -1;
     if (in_dtype != ORACLE_IN_BF16 && in_dtype != ORACLE_IN_F16) return -1;
@@ -140,10 +147,20 @@ int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
         double *y = Y + r * N;
         double *s = S + r * N;
         for (int64_t j = 0; j < N; ++j) { y[j] = 0.0; s[j] = 0.0; }
+        /* rmsnorm scale of row i (1 without normalisation) */
+        double scale = 1.0;
+        if (row_norm && K > 0) {
+            double ss = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = widen(a_col_major ? A[k * lda + i] : A[i * lda + k], in_dtype);
+                ss += a * a;
+            }
+            scale = 1.0 / sqrt(ss / (double)K + eps);
+        }
         /* k ascending, the same order for every element: y_ij accumulates
-         * a_ik*b_kj for k = 0, 1, ..., K-1. */
+         * a'_ik*b_kj for k = 0, 1, ..., K-1. */
         for (int64_t k = 0; k < K; ++k) {
-            const double a = widen(a_col_major ? A[k * lda + i] : A[i * lda + k], in_dtype);
+            const double a = scale * widen(a_col_major ? A[k * lda + i] : A[i * lda + k], in_dtype);
             const double *bk = b + k * N;
             for (int64_t j = 0; j < N; ++j) {
                 const double p = a * bk[j];
@@ -160,4 +177,16 @@ int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
     }
     free(b);
     return 0;
+}
+
+/* The GEMM without row normalisation. */
+int oracle_gemm(const uint16_t *A, int a_col_major, int64_t lda,
+                const uint16_t *B, int b_col_major, int64_t ldb,
+                const uint16_t *bias, int epi, int in_dtype,
+                int64_t M, int64_t N, int64_t K,
+                const int64_t *rows, int64_t n_rows,
+                double *Y, double *S)
+{
+    return oracle_gemm_norm(A, a_col_major, lda, B, b_col_major, ldb, bias, epi, in_dtype, 0, 0.0,
+                            M, N, K, rows, n_rows, Y, S);
 }

@@ -220,9 +220,32 @@ def pin_f16_gemm(orc):
     assert np.all(np.abs(y - ref) <= 1e-12 * S)
 
 
+def pin_row_norm(orc):
+    # rmsnorm(A) . B against numpy float64 (mean, sqrt and matmul are library routines)
+    rng = np.random.default_rng(23)
+    M, N, K, eps = 37, 29, 200, 1e-5
+    a = bits(rng.standard_normal((M, K)) * rng.uniform(0.1, 4.0, (M, 1)))
+    b = bits(rng.standard_normal((K, N)) / 8)
+    bias = bits(rng.standard_normal(N) / 10)
+    fa, fb = widen(a), widen(b)
+    an = fa / np.sqrt(np.mean(fa * fa, axis=1, keepdims=True) + eps)
+    y, S = orc.gemm(a, b, bias=bias, epi="bias", row_norm_eps=eps)
+    ref = an @ fb + widen(bias)[None, :]
+    assert np.all(np.abs(y - ref) <= 1e-12 * (np.abs(an) @ np.abs(fb) + 1.0))
+    assert np.allclose(S, np.abs(an) @ np.abs(fb), rtol=1e-12, atol=0)
+    # scale invariance: rmsnorm(c A) = rmsnorm(A) for c = 2^k (exact in bf16), up to eps
+    y2, _ = orc.gemm(bits(widen(a) * 4.0), b, bias=bias, epi="bias", row_norm_eps=0.0)
+    y1, _ = orc.gemm(a, b, bias=bias, epi="bias", row_norm_eps=0.0)
+    assert np.allclose(y1, y2, rtol=1e-12, atol=1e-12)
+    # a row of ones: mean square 1, scale 1/sqrt(1 + eps)
+    ones = bits(np.ones((1, K)))
+    y, _ = orc.gemm(ones, b, row_norm_eps=0.25)
+    assert np.allclose(y, fb.sum(axis=0, keepdims=True) / np.sqrt(1.25), rtol=1e-13, atol=0)
+
+
 PINS = [pin_golden, pin_identity_permutation, pin_rank1, pin_integer_exact,
         pin_fraction_bruteforce, pin_torch_float64, pin_gelu, pin_rows_and_degenerate,
-        pin_f16_widening_exhaustive, pin_f16_gemm]
+        pin_f16_widening_exhaustive, pin_f16_gemm, pin_row_norm]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -256,6 +279,8 @@ MUTANTS = {
     "gelu_scale": ("sqrt(2.0 / 3.14159265358979323846)", "sqrt(1.0 / 3.14159265358979323846)"),
     "s_not_abs": ("s[j] += fabs(p);", "s[j] += p;"),
     "a_k_reversed": ("A[i * lda + k], in_dtype);", "A[i * lda + (K - 1 - k)], in_dtype);"),
+    "norm_sum_not_mean": ("scale = 1.0 / sqrt(ss / (double)K + eps);", "scale = 1.0 / sqrt(ss + eps);"),
+    "norm_eps_dropped": ("scale = 1.0 / sqrt(ss / (double)K + eps);", "scale = 1.0 / sqrt(ss / (double)K);"),
     "f16_exponent_bias": ("v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);"),
     "f16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
 }
