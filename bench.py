@@ -45,7 +45,9 @@ WORKLOADS = {
     "skinny_bcast": ["skinny_bcast"],
     "skinny_bcast_ikbo": ["skinny_bcast_ikbo"],
     "dense_256": ["dense_256"],
+    "dense_4096_rmsnorm_bias_gelu": ["dense_4096_bias_gelu_rmsnorm"],
 }
+RMS_EPS = 1e-6
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 METRIC = "bf16 GEMM TFLOP/s and % of GB300 dense-BF16 peak (dense + grouped)"
@@ -180,11 +182,18 @@ class Part:
         self.grouped = name in wl.GROUPED_WORKLOADS
         self.bcast = name.endswith("_ikbo")          # in-kernel broadcast form of a repeated-row workload
         self.devcounts = name.endswith("_devcounts")  # MoE with the token counts in device memory
-        base = name[: -len("_ikbo")] if self.bcast else (name[: -len("_devcounts")] if self.devcounts else name)
+        self.rmsnorm = name.endswith("_rmsnorm")      # RMS normalisation of A's rows fused into the GEMM
+        base = name
+        for suffix in ("_ikbo", "_devcounts", "_rmsnorm"):
+            if base.endswith(suffix):
+                base = base[: -len(suffix)]
         self.grouped = self.grouped or self.devcounts
         self.case = wl.grouped_case(base) if self.grouped else wl.dense_case(base)
         self.flops = self.case.flops
         self.bytes = self.case.bcast_bytes if self.bcast else self.case.algorithmic_bytes
+        if self.rmsnorm:
+            # the row-statistics pass reads A once more and writes/reads one fp32 factor per row
+            self.bytes += self.case.M * self.case.K * 2 + 8 * self.case.M
         # the broadcast form stores far more than it computes: its roofline is the C write
         self.bound = "hbm" if (self.bcast or self.flops / self.bytes < 300) else "tensor"
 
@@ -198,8 +207,11 @@ class Part:
             return {"name": self.name, "M": c.M, "N": c.N, "K": c.K, "users": c.users.shape[0], "repeat": c.repeat,
                     "out": c.c_dtype, "epilogue": c.epi, "inputs": c.recipe,
                     "form": "in-kernel broadcast of the user rows (A not materialised)"}
-        return {"name": self.name, "M": c.M, "N": c.N, "K": c.K, "a": "col" if c.a_col_major else "row",
-                "b": "col" if c.b_col_major else "row", "out": c.c_dtype, "epilogue": c.epi, "inputs": c.recipe}
+        d = {"name": self.name, "M": c.M, "N": c.N, "K": c.K, "a": "col" if c.a_col_major else "row",
+             "b": "col" if c.b_col_major else "row", "out": c.c_dtype, "epilogue": c.epi, "inputs": c.recipe}
+        if self.rmsnorm:
+            d["norm"] = f"RMS of A's rows (eps {RMS_EPS}): row-statistics pass + row scale in the GEMM epilogue"
+        return d
 
     # -- device side
     def to_device(self, torch):
@@ -215,6 +227,8 @@ class Part:
         self.host["out"] = torch.empty((rows, c.N), dtype=dt).pin_memory()
         if self.devcounts:
             self.dev_counts = torch.tensor(c.counts, dtype=torch.int32, device="cuda")
+        if self.rmsnorm:
+            self.dev["row_scale"] = torch.empty(c.M, dtype=torch.float32, device="cuda")
         if self.grouped:
             import grouped_gemm_persistent_gb300 as tg
             self.table = tg.build_moe_table(self.dev["a"], self.dev["b"], c.counts, self.dev["out"],
@@ -232,6 +246,11 @@ class Part:
             tg.grouped_gemm_table(self.table, stream)
         elif self.bcast:
             tg.gemm_bcast(d["a"], d["b"], c.repeat, d["out"], bias=d.get("bias"), epilogue=c.epi, stream=stream)
+        elif self.rmsnorm:
+            b = d["b"].t() if c.b_col_major else d["b"]
+            tg.gemm_rmsnorm(d["a"], b, RMS_EPS, d["out"], row_scale=d["row_scale"], bias=d.get("bias"),
+                            epilogue=c.epi, stream=stream)
+            return 2   # row statistics + GEMM
         else:
             a = d["a"].t() if c.a_col_major else d["a"]
             b = d["b"].t() if c.b_col_major else d["b"]
@@ -240,7 +259,7 @@ class Part:
 
     def e2e_step(self, stream):
         for k, v in self.host.items():
-            if k != "out":
+            if k not in ("out", "row_scale"):
                 self.dev[k].copy_(v, non_blocking=True)
         n = self.launch(stream)
         self.host["out"].copy_(self.dev["out"], non_blocking=True)
@@ -261,7 +280,7 @@ class Part:
         rows = np.sort(rng.choice(c.M, size=min(n_rows, c.M), replace=False))
         bias = wl.bf16_bits(c.bias) if c.bias is not None else None
         oracle.gemm(wl.bf16_bits(c.a), wl.bf16_bits(c.b), a_col_major=c.a_col_major, b_col_major=c.b_col_major,
-                    bias=bias, epi=c.epi, rows=rows)
+                    bias=bias, epi=c.epi, rows=rows, row_norm_eps=RMS_EPS if self.rmsnorm else None)
         return 2 * len(rows) * c.N * c.K, len(rows)
 
 
@@ -419,7 +438,7 @@ def run_ours(args, parts_names):
     else:
         achieved = dp.flops / (dom_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": traffic, "kernel": f"gemm_kernel ({dp.name})",
+                    "frac": achieved / peak, "traffic": traffic, "kernel": ("row_rms_kernel + " if dp.rmsnorm else "") + f"gemm_kernel ({dp.name})",
                     "peak_source": f"{peak_src} {peak_kind}", "algorithmic_bytes": dp.bytes}
 
     cpu = None

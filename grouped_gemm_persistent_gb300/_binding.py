@@ -76,6 +76,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_gemm_bcast.argtypes = [vp, ci, i64, i64, i64, vp, ci, i64, vp, ci, i64, i64, i64, ci, vp, vp]
         lib.tg_moe_gemm.restype = ci
         lib.tg_moe_gemm.argtypes = [vp, i64, i64, i64, vp, ci, i64, i64, i64, i64, vp, ci, i64, vp, ci, vp, vp]
+        lib.tg_row_rms.restype = ci
+        lib.tg_row_rms.argtypes = [vp, i64, i64, i64, ctypes.c_float, vp, vp]
+        lib.tg_gemm_rmsnorm.restype = ci
+        lib.tg_gemm_rmsnorm.argtypes = [vp, i64, vp, ci, i64, vp, ci, i64, i64, i64, i64, ctypes.c_float, vp, ci,
+                                        vp, vp]
         lib.tg_grouped_gemm.restype = ci
         lib.tg_grouped_gemm.argtypes = [ctypes.POINTER(GroupProblem), ci, vp]
         lib.tg_grouped_gemm_noalloc.restype = ci
@@ -200,6 +205,63 @@ def gemm_bcast(a_user: torch.Tensor, b: torch.Tensor, repeat: int, out: torch.Te
     _check(load().tg_gemm_bcast(_ptr(a_user), la, lda, U, repeat, _ptr(b), lb, ldb, _ptr(out),
                                 _DTYPE_CODE[out.dtype], ldc, N, K, epi,
                                 _ptr(bias) if epi else None, _stream_handle(stream)))
+    return out
+
+
+def _row_major_bf16(a: torch.Tensor, name: str) -> int:
+    if a.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be torch.bfloat16")
+    la, lda = _matrix(a, name)
+    if la != ROW_MAJOR:
+        raise ValueError(f"{name} must be row-major")
+    return lda
+
+
+def row_rms(a: torch.Tensor, eps: float, out: torch.Tensor | None = None, *, stream=None) -> torch.Tensor:
+    """out[i] = 1 / sqrt(mean_k a[i, k]^2 + eps), fp32 [M], for a row-major bf16 ``a`` (tg_row_rms)."""
+    lda = _row_major_bf16(a, "a")
+    M, K = a.shape
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=a.device)
+    if out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 tensor of length M")
+    _check(load().tg_row_rms(_ptr(a), lda, M, K, float(eps), _ptr(out), _stream_handle(stream)))
+    return out
+
+
+def gemm_rmsnorm(a: torch.Tensor, b: torch.Tensor, eps: float, out: torch.Tensor | None = None, *,
+                 row_scale: torch.Tensor | None = None, bias: torch.Tensor | None = None, epilogue: str = "none",
+                 out_dtype: torch.dtype = torch.bfloat16, stream=None) -> torch.Tensor:
+    """out = epilogue(rmsnorm(a) @ b) with the normalisation fused into the GEMM (tg_gemm_rmsnorm).
+
+    ``a`` is row-major bf16 [M, K]; ``b`` bf16 [K, N] in either layout.  The row
+    factors land in ``row_scale`` (fp32 [M], allocated if not given).
+    """
+    lda = _row_major_bf16(a, "a")
+    if b.dtype != torch.bfloat16:
+        raise TypeError("b must be torch.bfloat16")
+    M, K = a.shape
+    K2, N = b.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: {K} vs {K2}")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    if out.dtype not in _DTYPE_CODE or tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N] bf16, fp16 or fp32")
+    if row_scale is None:
+        row_scale = torch.empty(M, dtype=torch.float32, device=a.device)
+    if row_scale.dtype != torch.float32 or row_scale.numel() != M or not row_scale.is_contiguous():
+        raise ValueError("row_scale must be a contiguous fp32 tensor of length M")
+    lb, ldb = _matrix(b, "b")
+    lc, ldc = _matrix(out, "out")
+    if lc != ROW_MAJOR:
+        raise ValueError("out must be row-major")
+    epi = EPILOGUES[epilogue]
+    if epi and (bias is None or bias.dtype != torch.bfloat16 or bias.numel() != N or not bias.is_contiguous()):
+        raise ValueError("this epilogue needs a contiguous bf16 bias of length N")
+    _check(load().tg_gemm_rmsnorm(_ptr(a), lda, _ptr(b), lb, ldb, _ptr(out), _DTYPE_CODE[out.dtype], ldc, M, N, K,
+                                  float(eps), _ptr(row_scale), epi, _ptr(bias) if epi else None,
+                                  _stream_handle(stream)))
     return out
 
 

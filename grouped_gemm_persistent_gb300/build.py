@@ -29,7 +29,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                 "--expt-relaxed-constexpr"]
 
-UNITS = [("tg_api", "tg_api.cu", [])] + [
+UNITS = [("tg_api", "tg_api.cu", []), ("tg_norm", "tg_norm.cu", [])] + [
     (f"tg_inst_f{f}_m{m}", "tg_inst.cu", [f"-DTG_INST_F32={f}", f"-DTG_INST_MODE={m}"])
     for f in (0, 1) for m in (0, 1, 2)
 ]
@@ -54,7 +54,8 @@ def _digest(extra_flags) -> str:
                 h.update(name.encode())
                 with open(p, "rb") as f:
                     h.update(f.read())
-    h.update(" ".join(FLAGS + list(extra_flags)).encode())
+    # flags with the checkout's location taken out, so a copy elsewhere hashes the same
+    h.update(" ".join(FLAGS + list(extra_flags)).replace(ROOT, "<root>").encode())
     return h.hexdigest()
 
 

@@ -184,6 +184,7 @@ struct Prob {
     tg_epilogue epi;
     const void* bias;
     tg_dtype ab;          // element type of A, B and bias: TG_BF16 or TG_F16
+    const float* row_scale = nullptr;   // optional per-row factor on the accumulator (RMS norm)
 };
 
 Prob prob_of(const tg_group_problem& t) {
@@ -354,6 +355,7 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     s = make_map(&out->tma_c, c_type, q.C, q.N, q.M, q.ldc * (f32 ? 4 : 2), v.cw, 32, "C", g);
     if (s != TG_OK) return s;
     out->bias = q.epi != TG_EPI_NONE ? q.bias : nullptr;
+    out->row_scale = q.row_scale;
     out->idesc = tg::ptx::idesc_f32_acc(v.tile_m, v.bn, q.la == TG_COL_MAJOR, q.lb == TG_ROW_MAJOR, ab_f16);
     out->flags = (q.cd == TG_F16 ? tg::FLAG_C_F16 : 0u) | (ab_f16 ? tg::FLAG_BIAS_F16 : 0u);
     out->M = static_cast<int32_t>(q.M);
@@ -487,6 +489,39 @@ tg_status tg_gemm(const void* A, tg_layout layout_a, int64_t lda, const void* B,
                   void* C, tg_dtype c_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K, tg_epilogue epi,
                   const void* bias, tg_stream_t stream) {
     return dense_gemm(Prob{A, layout_a, lda, B, layout_b, ldb, C, c_dtype, ldc, M, N, K, epi, bias, TG_BF16}, stream);
+}
+
+tg_status tg_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps, float* r, tg_stream_t stream) {
+    if (M < 0 || K < 0) return fail(TG_ERR_INVALID_ARG, "negative size M=%lld K=%lld", (long long)M, (long long)K);
+    if (M == 0) return TG_OK;
+    if (!r) return fail(TG_ERR_INVALID_ARG, "r is NULL");
+    if (!(eps >= 0.0f)) return fail(TG_ERR_INVALID_ARG, "eps must be a non-negative number");
+    if (K > 0) {
+        if (!A) return fail(TG_ERR_INVALID_ARG, "A is NULL");
+        if (lda < K) return fail(TG_ERR_INVALID_ARG, "lda=%lld < K=%lld", (long long)lda, (long long)K);
+        if (!aligned16(A) || (lda * 2) % 16)
+            return fail(TG_ERR_UNSUPPORTED, "A must be 16-byte aligned with lda a multiple of 8");
+    }
+    if (reinterpret_cast<uintptr_t>(r) & 3u) return fail(TG_ERR_INVALID_ARG, "r is not 4-byte aligned");
+    DeviceState* d = nullptr;
+    tg_status s = device_state(&d);
+    if (s != TG_OK) return s;
+    cudaError_t e = tg::launch_row_rms(A, lda, M, K, eps, r, d->sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "row statistics launch");
+    return TG_OK;
+}
+
+tg_status tg_gemm_rmsnorm(const void* A, int64_t lda, const void* B, tg_layout layout_b, int64_t ldb, void* C,
+                          tg_dtype c_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K, float eps, float* row_scale,
+                          tg_epilogue epi, const void* bias, tg_stream_t stream) {
+    Prob q{A, TG_ROW_MAJOR, lda, B, layout_b, ldb, C, c_dtype, ldc, M, N, K, epi, bias, TG_BF16};
+    tg_status s = check(q, 0);
+    if (s != TG_OK) return s;
+    if (M == 0 || N == 0) return TG_OK;
+    if (!row_scale) return fail(TG_ERR_INVALID_ARG, "row_scale is NULL");
+    if ((s = tg_row_rms(A, lda, M, K, eps, row_scale, stream)) != TG_OK) return s;
+    q.row_scale = row_scale;
+    return dense_gemm(q, stream);
 }
 
 tg_status tg_gemm_ex(const tg_group_problem* problem, tg_stream_t stream) {

@@ -72,6 +72,7 @@ struct alignas(128) Problem {
     CUtensorMap tma_b;
     CUtensorMap tma_c;
     const void* bias;       // bf16 or fp16 [N] (FLAG_BIAS_F16)
+    const float* row_scale;   // optional fp32 [M]: row i of the accumulator is multiplied by it (RMS norm)
     int64_t tile_begin;   // global index of this problem's first tile
     int32_t M, N, K;
     int32_t epi;
@@ -657,6 +658,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             const bool tracer = p.trace_tiles && lane == 0 && ew == 0 && leader && t < p.trace_tiles_cap;
             if (tracer) p.trace_tiles[4 * t + 2] = ptx::globaltimer_ns();
 
+            // RMS normalisation of A's row: one factor per accumulator row (this lane's row)
+            float rs = 1.0f;
+            if (pr.row_scale && row0 + lane < row_limit) rs = __ldg(pr.row_scale + row0 + lane);
+
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             constexpr int CHUNKS = BN / Cfg::CW;
 #pragma unroll 1
@@ -686,6 +691,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 }
                 const int n_chunk = tc.n0 + c * Cfg::CW;
                 if (!active || n_chunk >= pr.N) continue;
+                if (pr.row_scale) {
+#pragma unroll
+                    for (int i = 0; i < Cfg::CW; ++i) v[i] *= rs;
+                }
 
                 if (epi != EPI_NONE) {
                     // bias[n_chunk .. n_chunk + CW): the same values for every lane (broadcast loads)

@@ -19,6 +19,10 @@ cudaError_t launch(const Params& p, int grid, cudaStream_t stream);
 template <class Cfg>
 cudaError_t resident_units(int* units);
 
+// r[i] = 1 / sqrt(mean_k A[i][k]^2 + eps) for a row-major bf16 A (tg_norm.cu).
+cudaError_t launch_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps, float* r, int sms,
+                           cudaStream_t stream);
+
 }  // namespace tg
 
 // Every (BN, CTA_GROUP, A_MN, B_MN) combination for one (C_F32, MODE) pair

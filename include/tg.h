@@ -122,6 +122,27 @@ tg_status tg_gemm_bcast(const void *A_user, tg_layout layout_a, int64_t lda, int
                         tg_stream_t stream);
 
 /*
+ * tg_row_rms - r[i] = 1 / sqrt((1/K) sum_k A[i][k]^2 + eps) for a row-major bf16
+ * A [M, K] (lda >= K, 16-byte aligned rows); r is a DEVICE fp32 [M].  Sums run
+ * in fp32 in a fixed order (deterministic).  K == 0 gives r = 1 / sqrt(eps).
+ */
+tg_status tg_row_rms(const void *A, int64_t lda, int64_t M, int64_t K, float eps, float *r, tg_stream_t stream);
+
+/*
+ * tg_gemm_rmsnorm - C = epilogue(rmsnorm(A) . B), the normalisation fused
+ * into the GEMM (the TLX pages' "fuse the norm into the GEMM" idea): since
+ * rmsnorm(A) = diag(r) A, the product is computed on A as stored and row i of
+ * the fp32 accumulator is scaled by r_i in the epilogue, before bias and GELU;
+ * the normalised A is never written or read back.  r comes from tg_row_rms
+ * (one read of A) and is left in row_scale (DEVICE fp32 [M]) for reuse.  A
+ * gain vector gamma folds into B: rmsnorm_gamma(A) . B = rmsnorm(A) . diag(gamma) B.
+ * A is row-major bf16; other arguments as tg_gemm.
+ */
+tg_status tg_gemm_rmsnorm(const void *A, int64_t lda, const void *B, tg_layout layout_b, int64_t ldb,
+                          void *C, tg_dtype c_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                          float eps, float *row_scale, tg_epilogue epi, const void *bias, tg_stream_t stream);
+
+/*
  * One problem of a grouped GEMM: C_g = epilogue_g(A_g . B_g), fields as in
  * tg_gemm.  Problems are independent and may differ in every field; a problem
  * with M == 0 or N == 0 (an expert that received no tokens) is skipped and its

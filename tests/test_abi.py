@@ -176,3 +176,27 @@ def test_moe_argument_checks(lib):
     assert moe(N=60) == tg.TG_ERR_UNSUPPORTED                           # N % 8
     assert moe(stride=64 * 63) == tg.TG_ERR_INVALID_ARG                 # one expert does not fit its stride
     assert moe(T=-1) == tg.TG_ERR_INVALID_ARG
+
+
+def test_rmsnorm_argument_checks(lib):
+    f = ctypes.c_float
+    def rms(A=ALIGNED, lda=64, M=64, K=64, eps=1e-6, r=0x40000):
+        return lib.tg_row_rms(A, lda, M, K, f(eps), r, None)
+    assert rms(M=0) == tg.TG_OK                                         # nothing to do
+    assert rms(M=-1) == tg.TG_ERR_INVALID_ARG
+    assert rms(r=None) == tg.TG_ERR_INVALID_ARG
+    assert rms(r=0x40002) == tg.TG_ERR_INVALID_ARG                      # fp32 output, 4-byte aligned
+    assert rms(eps=-1.0) == tg.TG_ERR_INVALID_ARG
+    assert rms(eps=float("nan")) == tg.TG_ERR_INVALID_ARG
+    assert rms(A=None) == tg.TG_ERR_INVALID_ARG
+    assert rms(lda=32) == tg.TG_ERR_INVALID_ARG                         # lda < K
+    assert rms(lda=68) == tg.TG_ERR_UNSUPPORTED                         # rows not 16-byte aligned
+    assert rms(A=ALIGNED + 2) == tg.TG_ERR_UNSUPPORTED
+
+    def fused(M=64, N=64, K=64, A=ALIGNED, rs=0x40000, ldb=64, epi=0, bias=NULL):
+        return lib.tg_gemm_rmsnorm(A, 64, ALIGNED_B, 0, ldb, ALIGNED_C, 0, 64, M, N, K, f(1e-6), rs, epi, bias, None)
+    assert fused(M=0) == tg.TG_OK and fused(N=0) == tg.TG_OK
+    assert fused(rs=None) == tg.TG_ERR_INVALID_ARG
+    assert fused(A=None) == tg.TG_ERR_INVALID_ARG
+    assert fused(ldb=32) == tg.TG_ERR_INVALID_ARG
+    assert fused(epi=1) == tg.TG_ERR_INVALID_ARG                        # bias epilogue without a bias
