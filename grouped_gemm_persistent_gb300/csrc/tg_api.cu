@@ -520,7 +520,8 @@ tg_status tg_gemm_rmsnorm(const void* A, int64_t lda, const void* B, tg_layout l
     if (M == 0 || N == 0) return TG_OK;
     if (!row_scale) return fail(TG_ERR_INVALID_ARG, "row_scale is NULL");
     if ((s = tg_row_rms(A, lda, M, K, eps, row_scale, stream)) != TG_OK) return s;
-    q.row_scale = row_scale;
+    // with K == 0 the product is 0 whatever r is (r may be infinite when eps == 0): no scale
+    q.row_scale = K > 0 ? row_scale : nullptr;
     return dense_gemm(q, stream);
 }
 

@@ -136,7 +136,8 @@ tg_status tg_row_rms(const void *A, int64_t lda, int64_t M, int64_t K, float eps
  * the normalised A is never written or read back.  r comes from tg_row_rms
  * (one read of A) and is left in row_scale (DEVICE fp32 [M]) for reuse.  A
  * gain vector gamma folds into B: rmsnorm_gamma(A) . B = rmsnorm(A) . diag(gamma) B.
- * A is row-major bf16; other arguments as tg_gemm.
+ * A is row-major bf16; other arguments as tg_gemm.  With K == 0 the result is
+ * epilogue(0) (an empty row normalises to an empty row), even when eps == 0.
  */
 tg_status tg_gemm_rmsnorm(const void *A, int64_t lda, const void *B, tg_layout layout_b, int64_t ldb,
                           void *C, tg_dtype c_dtype, int64_t ldc, int64_t M, int64_t N, int64_t K,

@@ -208,7 +208,8 @@ def compare(c: np.ndarray, y: np.ndarray, s: np.ndarray, bias_abs: np.ndarray | 
     ratio = err / bnd
     scale = s if bias_abs is None else s + bias_abs[None, :]
     tight = err / (2.0 ** -8 * np.abs(y) + 2.0 ** -11 * scale + 1e-30)
-    worst = np.unravel_index(np.nanargmax(ratio), ratio.shape) if ratio.size else None
+    # NaN ranks as the worst element
+    worst = np.unravel_index(np.argmax(np.where(np.isnan(ratio), np.inf, ratio)), ratio.shape) if ratio.size else None
     return {
         "ok": bool(not bad.any()),
         "n_bad": int(bad.sum()),
