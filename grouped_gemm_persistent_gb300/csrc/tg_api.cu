@@ -562,6 +562,7 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream) {
     p.total_tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
     p.band = pick_band(p.dense.tiles_n, units);
     base_params(&p, d);
+    p.pdl = q.row_scale != nullptr;   // the row factors come from the kernel enqueued just before
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -615,6 +616,7 @@ tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int
     p.total_tiles = tiles * replicas;
     p.band = pick_band(p.dense.tiles_n, units);
     base_params(&p, d);
+    p.pdl = q.row_scale != nullptr;   // the row factors come from the kernel enqueued just before
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
 }
 

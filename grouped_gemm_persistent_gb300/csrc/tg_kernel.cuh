@@ -117,6 +117,10 @@ struct Params {
     int64_t moe_rows;           // T: rows of A and C; the counts must sum to at most T
     void* moe_c;                // C base pointer, for rows stored without TMA
     int64_t moe_ldc;            // elements per row of C
+    // Host side only: launch as a programmatic dependent of the kernel before it in the
+    // stream (the row-statistics pass of the fused RMS norm).  Only the epilogue reads
+    // that kernel's output, after griddepcontrol.wait; set-up and main loop overlap it.
+    int32_t pdl;
 };
 
 // MODE: 0 dense (tensor maps in parameter space), 1 grouped (problem table in
@@ -660,7 +664,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             // RMS normalisation of A's row: one factor per accumulator row (this lane's row)
             float rs = 1.0f;
-            if (pr.row_scale && row0 + lane < row_limit) rs = __ldg(pr.row_scale + row0 + lane);
+            if (pr.row_scale) {
+                ptx::grid_dependency_wait();      // the factors come from the kernel launched before this one
+                if (row0 + lane < row_limit) rs = pr.row_scale[row0 + lane];
+            }
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             constexpr int CHUNKS = BN / Cfg::CW;

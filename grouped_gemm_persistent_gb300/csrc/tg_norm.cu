@@ -16,10 +16,14 @@
 namespace tg {
 
 constexpr int RMS_WARPS = 8;   // rows in flight per 256-thread block
+constexpr int UNROLL = 4;      // 16-byte loads in flight per lane
 
 __global__ void __launch_bounds__(RMS_WARPS * 32) row_rms_kernel(const uint16_t* __restrict__ A, int64_t lda,
                                                                   int64_t M, int64_t K, float eps,
                                                                   float* __restrict__ r) {
+    // the fused GEMM launched after this kernel may start its set-up and main loop now;
+    // it waits for this grid's completion only before reading r
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RMS_WARPS;
@@ -28,8 +32,7 @@ __global__ void __launch_bounds__(RMS_WARPS * 32) row_rms_kernel(const uint16_t*
         const uint16_t* a = A + row * lda;
         const uint4* av = reinterpret_cast<const uint4*>(a);
         float ss = 0.0f;
-        for (int64_t v = lane; v < kvec; v += 32) {
-            const uint4 w = __ldg(av + v);
+        auto add = [&ss](const uint4& w) {
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -38,7 +41,17 @@ __global__ void __launch_bounds__(RMS_WARPS * 32) row_rms_kernel(const uint16_t*
                 ss = fmaf(lo, lo, ss);
                 ss = fmaf(hi, hi, ss);
             }
+        };
+        int64_t v = lane;
+        // UNROLL independent 16-byte loads in flight per lane, then the remainder
+        for (; v + 32 * (UNROLL - 1) < kvec; v += 32 * UNROLL) {
+            uint4 w[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) w[u] = __ldg(av + v + 32 * u);
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) add(w[u]);
         }
+        for (; v < kvec; v += 32) add(__ldg(av + v));
         for (int64_t k = kvec * 8 + lane; k < K; k += 32) {
             const float x = __uint_as_float(static_cast<uint32_t>(__ldg(a + k)) << 16);
             ss = fmaf(x, x, ss);

@@ -290,6 +290,13 @@ __host__ __device__ constexpr uint32_t idesc_f32_acc(uint32_t M, uint32_t N, boo
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start once every block of the kernel before it has called
+// launch_dependents (or exited); wait returns when that kernel has completed and
+// its memory operations are visible.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------------------
 // math
 
