@@ -375,7 +375,8 @@ def run_ours(args, parts_names):
         barrier(world)
         torch.cuda.synchronize()
         for i in range(args.steps):
-            flush.zero_()                     # L2 flush, outside the timed events
+            if not args.warm:
+                flush.zero_()                 # L2 flush, outside the timed events
             ev[i][0].record(stream)
             for j, p in enumerate(parts):
                 launches += p.launch(stream)
@@ -460,7 +461,7 @@ def run_ours(args, parts_names):
         "metric": METRIC, "value": agg["value_tflops"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "parts": parts_out, "l2": "flushed between steps (256 MiB write)",
+        "config": {"workload": args.workload, "parts": parts_out, "l2": "warm (not flushed between steps)" if args.warm else "flushed between steps (256 MiB write)",
                    "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
                    "frac_of_peak": agg["value_tflops"] / (world * peak)},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
@@ -482,6 +483,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=HEADLINE)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--warm", action="store_true",
+                    help="do not flush L2 between timed steps (reported as warm; the default is cold)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
