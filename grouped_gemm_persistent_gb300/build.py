@@ -2,7 +2,7 @@
 
     python -m grouped_gemm_persistent_gb300.build [--force] [--verbose-ptxas]
 
-Translation units compile in parallel: the host API once, the kernel
+Translation units compile in parallel: the host API and the auxiliary kernels once, the kernel
 instantiations once per (output dtype, dense / grouped / MoE) pair.  The result is
 grouped_gemm_persistent_gb300/libtg.so; objects go to
 grouped_gemm_persistent_gb300/_build/.  A rebuild happens only when a source
@@ -29,7 +29,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
                 "--expt-relaxed-constexpr"]
 
-UNITS = [("tg_api", "tg_api.cu", []), ("tg_norm", "tg_norm.cu", [])] + [
+UNITS = [("tg_api", "tg_api.cu", []), ("tg_aux", "tg_aux.cu", [])] + [
     (f"tg_inst_f{f}_m{m}", "tg_inst.cu", [f"-DTG_INST_F32={f}", f"-DTG_INST_MODE={m}"])
     for f in (0, 1) for m in (0, 1, 2)
 ]

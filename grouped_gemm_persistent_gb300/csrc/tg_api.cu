@@ -383,7 +383,7 @@ void base_params(Params* p, DeviceState* d) {
 }
 
 tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t stream) {
-    int64_t want = p.total_tiles < units ? p.total_tiles : units;
+    int64_t want = p.total_units < units ? p.total_units : units;
     const int grid = static_cast<int>(want) * v.cta_group;
     cudaError_t e = v.launch(p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -477,7 +477,30 @@ thread_local tg::Problem t_noalloc_host[TG_NOALLOC_MAX_PROBLEMS];
 }  // namespace
 
 namespace {
-tg_status dense_gemm(const Prob& q, tg_stream_t stream);
+// Row statistics launched just before a dense GEMM (the fused RMS normalisation).
+struct RowPass {
+    const void* A;
+    int64_t lda, M, K;
+    float eps;
+    float* r;
+};
+
+tg_status check_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps, const float* r) {
+    if (M < 0 || K < 0) return fail(TG_ERR_INVALID_ARG, "negative size M=%lld K=%lld", (long long)M, (long long)K);
+    if (M == 0) return TG_OK;
+    if (!r) return fail(TG_ERR_INVALID_ARG, "r is NULL");
+    if (!(eps >= 0.0f)) return fail(TG_ERR_INVALID_ARG, "eps must be a non-negative number");
+    if (K > 0) {
+        if (!A) return fail(TG_ERR_INVALID_ARG, "A is NULL");
+        if (lda < K) return fail(TG_ERR_INVALID_ARG, "lda=%lld < K=%lld", (long long)lda, (long long)K);
+        if (!aligned16(A) || (lda * 2) % 16)
+            return fail(TG_ERR_UNSUPPORTED, "A must be 16-byte aligned with lda a multiple of 8");
+    }
+    if (reinterpret_cast<uintptr_t>(r) & 3u) return fail(TG_ERR_INVALID_ARG, "r is not 4-byte aligned");
+    return TG_OK;
+}
+
+tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre = nullptr);
 }  // namespace
 
 // ========================================================================================
@@ -492,20 +515,10 @@ tg_status tg_gemm(const void* A, tg_layout layout_a, int64_t lda, const void* B,
 }
 
 tg_status tg_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps, float* r, tg_stream_t stream) {
-    if (M < 0 || K < 0) return fail(TG_ERR_INVALID_ARG, "negative size M=%lld K=%lld", (long long)M, (long long)K);
-    if (M == 0) return TG_OK;
-    if (!r) return fail(TG_ERR_INVALID_ARG, "r is NULL");
-    if (!(eps >= 0.0f)) return fail(TG_ERR_INVALID_ARG, "eps must be a non-negative number");
-    if (K > 0) {
-        if (!A) return fail(TG_ERR_INVALID_ARG, "A is NULL");
-        if (lda < K) return fail(TG_ERR_INVALID_ARG, "lda=%lld < K=%lld", (long long)lda, (long long)K);
-        if (!aligned16(A) || (lda * 2) % 16)
-            return fail(TG_ERR_UNSUPPORTED, "A must be 16-byte aligned with lda a multiple of 8");
-    }
-    if (reinterpret_cast<uintptr_t>(r) & 3u) return fail(TG_ERR_INVALID_ARG, "r is not 4-byte aligned");
+    tg_status s = check_row_rms(A, lda, M, K, eps, r);
+    if (s != TG_OK || M == 0) return s;
     DeviceState* d = nullptr;
-    tg_status s = device_state(&d);
-    if (s != TG_OK) return s;
+    if ((s = device_state(&d)) != TG_OK) return s;
     cudaError_t e = tg::launch_row_rms(A, lda, M, K, eps, r, d->sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "row statistics launch");
     return TG_OK;
@@ -519,10 +532,11 @@ tg_status tg_gemm_rmsnorm(const void* A, int64_t lda, const void* B, tg_layout l
     if (s != TG_OK) return s;
     if (M == 0 || N == 0) return TG_OK;
     if (!row_scale) return fail(TG_ERR_INVALID_ARG, "row_scale is NULL");
-    if ((s = tg_row_rms(A, lda, M, K, eps, row_scale, stream)) != TG_OK) return s;
+    if ((s = check_row_rms(A, lda, M, K, eps, row_scale)) != TG_OK) return s;
     // with K == 0 the product is 0 whatever r is (r may be infinite when eps == 0): no scale
     q.row_scale = K > 0 ? row_scale : nullptr;
-    return dense_gemm(q, stream);
+    const RowPass pre{A, lda, M, K, eps, row_scale};
+    return dense_gemm(q, stream, &pre);
 }
 
 tg_status tg_gemm_ex(const tg_group_problem* problem, tg_stream_t stream) {
@@ -534,7 +548,35 @@ tg_status tg_gemm_ex(const tg_group_problem* problem, tg_stream_t stream) {
 
 namespace {
 
-tg_status dense_gemm(const Prob& q, tg_stream_t stream) {
+// Split of the last, partial wave of a dense launch: its R tiles are cut into S
+// K-ranges (slices) so R * S work units spread over the resident CTAs (pairs).
+constexpr int kMinSliceKb = 4;    // k-blocks (of 64) per slice at least
+constexpr int kMaxSlices = 8;
+
+struct SplitPlan {
+    int64_t first = 0;   // first split tile
+    int tiles = 0;       // R
+    int slices = 0;      // S (0: no split)
+};
+
+SplitPlan plan_split(int64_t tiles, int units, int k_blocks) {
+    SplitPlan sp;
+    const char* env = std::getenv("TG_SPLIT_TAIL");
+    if (env && env[0] == '0') return sp;
+    if (units <= 0 || k_blocks < 2 * kMinSliceKb) return sp;
+    const int64_t R = tiles % units;
+    if (R == 0) return sp;
+    int64_t S = units / R;
+    if (S > k_blocks / kMinSliceKb) S = k_blocks / kMinSliceKb;
+    if (S > kMaxSlices) S = kMaxSlices;
+    if (S < 2) return sp;
+    sp.first = tiles - R;
+    sp.tiles = static_cast<int>(R);
+    sp.slices = static_cast<int>(S);
+    return sp;
+}
+
+tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
     const void* B = q.B;
     const tg_layout layout_a = q.la, layout_b = q.lb;
     const tg_dtype c_dtype = q.cd;
@@ -559,11 +601,42 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream) {
     p.dense.tile_begin = 0;
     p.problems = nullptr;
     p.num_problems = 1;
-    p.total_tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
+    const int64_t tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
+    p.total_units = tiles;
     p.band = pick_band(p.dense.tiles_n, units);
     base_params(&p, d);
-    p.pdl = q.row_scale != nullptr;   // the row factors come from the kernel enqueued just before
-    return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const SplitPlan sp = plan_split(tiles, units, p.dense.k_blocks);
+    void* ws = nullptr;
+    int n_counters = 0;
+    if (sp.slices > 1) {
+        // partial sums of every slice, then one arrival counter per (split tile, CTA, epilogue warp)
+        const size_t partial = static_cast<size_t>(sp.tiles) * sp.slices * v.tile_m * v.bn * sizeof(float);
+        n_counters = sp.tiles * v.cta_group * tg::NUM_EPI_WARPS;
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, partial + n_counters * sizeof(uint32_t), d->pool, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(split partials)");
+        p.sk_first = sp.first;
+        p.sk_tiles = sp.tiles;
+        p.sk_slices = sp.slices;
+        p.sk_partial = static_cast<float*>(ws);
+        p.sk_count = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + partial);
+        p.total_units = sp.first + static_cast<int64_t>(sp.tiles) * sp.slices;
+    }
+    // the kernel before the GEMM: the row pass (which also zeroes the counters) or the counter reset;
+    // the GEMM follows it as a programmatic dependent and waits for it only where it reads its output
+    cudaError_t e = cudaSuccess;
+    if (pre) e = tg::launch_row_rms(pre->A, pre->lda, pre->M, pre->K, pre->eps, pre->r, d->sms, st, p.sk_count,
+                                    n_counters);
+    else if (n_counters) e = tg::launch_clear_counters(p.sk_count, n_counters, st);
+    s = e == cudaSuccess ? TG_OK : cuda_fail(e, pre ? "row statistics launch" : "counter reset launch");
+    p.pdl = (pre != nullptr || n_counters > 0) ? 1 : 0;
+    if (s == TG_OK) s = enqueue(p, v, units, st);
+    if (ws) {
+        e = cudaFreeAsync(ws, st);   // stream-ordered: released after the GEMM has run
+        if (e != cudaSuccess && s == TG_OK) s = cuda_fail(e, "cudaFreeAsync(split partials)");
+    }
+    return s;
 }
 
 }  // namespace
@@ -613,10 +686,9 @@ tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int
     p.dense.replicas = static_cast<int32_t>(replicas);
     p.dense.tile_begin = 0;
     p.num_problems = 1;
-    p.total_tiles = tiles * replicas;
+    p.total_units = tiles * replicas;
     p.band = pick_band(p.dense.tiles_n, units);
     base_params(&p, d);
-    p.pdl = q.row_scale != nullptr;   // the row factors come from the kernel enqueued just before
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -678,7 +750,7 @@ tg_status tg_moe_gemm(const void* A, int64_t lda, int64_t T, int64_t K, const vo
         if (s != TG_OK) return s;
     }
     p.num_problems = 1;
-    p.total_tiles = 0;   // the kernel derives it from the device counts
+    p.total_units = 0;   // the kernel derives it from the device counts
     p.band = pick_band(p.dense.tiles_n, units);
     p.moe_counts = counts;
     p.moe_groups = static_cast<int32_t>(G);
@@ -758,7 +830,7 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
         std::memset(&p, 0, sizeof p);
         p.problems = static_cast<const Problem*>(ws);
         p.num_problems = static_cast<int32_t>(host.size());
-        p.total_tiles = tiles;
+        p.total_units = tiles;
         p.band = pick_band(max_tiles_n, units);
         t_withhold = withhold;
         base_params(&p, d);
@@ -846,7 +918,7 @@ tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_strea
         std::memset(&p, 0, sizeof p);
         p.problems = d->table + offset;
         p.num_problems = n;
-        p.total_tiles = tiles;
+        p.total_units = tiles;
         p.band = pick_band(max_tiles_n, units);
         p.err = d->err;
         p.wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;

@@ -1,4 +1,6 @@
-// tg_norm.cu - row statistics for the RMS normalisation fused into the GEMM.
+// tg_aux.cu - the small kernels launched before a GEMM: row statistics for the RMS
+// normalisation fused into the GEMM, and the reset of the arrival counters of
+// split tiles.
 //
 // rmsnorm(A) . B = diag(r) (A . B) with r_i = 1 / sqrt(mean_k A_ik^2 + eps): the
 // normalisation is a per-row scale that the GEMM epilogue applies to its fp32
@@ -18,12 +20,20 @@ namespace tg {
 constexpr int RMS_WARPS = 8;   // rows in flight per 256-thread block
 constexpr int UNROLL = 4;      // 16-byte loads in flight per lane
 
+// Counters of split tiles start at zero in every GEMM launch that uses them.
+__device__ __forceinline__ void clear_counters(uint32_t* counters, int n) {
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n; i += blockDim.x) counters[i] = 0u;
+}
+
 __global__ void __launch_bounds__(RMS_WARPS * 32) row_rms_kernel(const uint16_t* __restrict__ A, int64_t lda,
                                                                   int64_t M, int64_t K, float eps,
-                                                                  float* __restrict__ r) {
+                                                                  float* __restrict__ r, uint32_t* counters,
+                                                                  int n_counters) {
     // the fused GEMM launched after this kernel may start its set-up and main loop now;
-    // it waits for this grid's completion only before reading r
+    // it waits for this grid's completion only before reading r (and the counters)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    clear_counters(counters, n_counters);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RMS_WARPS;
@@ -63,13 +73,24 @@ __global__ void __launch_bounds__(RMS_WARPS * 32) row_rms_kernel(const uint16_t*
     }
 }
 
+__global__ void __launch_bounds__(256) clear_counters_kernel(uint32_t* counters, int n) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    clear_counters(counters, n);
+}
+
+cudaError_t launch_clear_counters(uint32_t* counters, int n, cudaStream_t stream) {
+    clear_counters_kernel<<<1, 256, 0, stream>>>(counters, n);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps, float* r, int sms,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, uint32_t* counters, int n_counters) {
     int64_t blocks = (M + RMS_WARPS - 1) / RMS_WARPS;
     const int64_t cap = static_cast<int64_t>(sms) * 8;   // a few resident blocks per SM, grid-stride beyond
     if (blocks > cap) blocks = cap;
     row_rms_kernel<<<static_cast<unsigned>(blocks), RMS_WARPS * 32, 0, stream>>>(static_cast<const uint16_t*>(A), lda,
-                                                                                  M, K, eps, r);
+                                                                                  M, K, eps, r, counters,
+                                                                                  n_counters);
     return cudaGetLastError();
 }
 

@@ -98,7 +98,7 @@ struct Params {
     const Problem* problems;    // grouped launch: device array written by the host
     int32_t num_problems;
     int32_t band;               // raster band width in N-tiles
-    int64_t total_tiles;
+    int64_t total_units;        // work units: whole tiles, plus one per extra slice of a split tile
     ErrorRecord* err;
     uint64_t wait_budget_ns;
     int64_t withhold_kb;        // test hook, -1 = off (see tg_debug_withhold_stage)
@@ -121,6 +121,17 @@ struct Params {
     // stream (the row-statistics pass of the fused RMS norm).  Only the epilogue reads
     // that kernel's output, after griddepcontrol.wait; set-up and main loop overlap it.
     int32_t pdl;
+    // Split tiles (dense only).  Tiles [sk_first, sk_first + sk_tiles) - the last,
+    // partial wave of the persistent schedule - are each computed by sk_slices work
+    // units over consecutive K-ranges, run by different CTAs (pairs) at the same time.
+    // Every slice writes its fp32 partial sums to sk_partial; the slice that arrives
+    // last at sk_count (zeroed by the kernel launched just before) adds the partials
+    // in slice order and runs the epilogue, so results do not depend on timing.
+    int64_t sk_first;
+    int32_t sk_tiles;
+    int32_t sk_slices;          // 0: no split
+    float* sk_partial;          // [sk_tiles][sk_slices][CTA_GROUP][4 warps][BN/4][32 lanes][4]
+    uint32_t* sk_count;         // [sk_tiles][CTA_GROUP][4 warps]
 };
 
 // MODE: 0 dense (tensor maps in parameter space), 1 grouped (problem table in
@@ -241,6 +252,33 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
         c.row_end = mt.row_off[g + 1];
     }
     return c;
+}
+
+// A work unit: a whole tile, or one K-range (slice) of a split tile.
+struct Work {
+    int64_t t;    // tile
+    int kb0;      // split tiles: k-blocks [kb0, kb1); whole tiles use the problem's k_blocks
+    int kb1;
+    int slice;
+    int tail;     // index among the split tiles, or -1 for a whole tile
+};
+
+template <class Cfg>
+__device__ __forceinline__ Work work_of(const Params& p, int64_t u) {
+    Work w{u, 0, 0, 0, -1};
+    if constexpr (!Cfg::GROUPED && !Cfg::MOE) {
+        if (p.sk_slices > 1 && u >= p.sk_first) {
+            const int64_t v = u - p.sk_first;
+            const int S = p.sk_slices;
+            const int kbs = p.dense.k_blocks;
+            w.tail = static_cast<int>(v % p.sk_tiles);
+            w.slice = static_cast<int>(v / p.sk_tiles);
+            w.t = p.sk_first + w.tail;
+            w.kb0 = static_cast<int>(static_cast<int64_t>(w.slice) * kbs / S);
+            w.kb1 = static_cast<int>(static_cast<int64_t>(w.slice + 1) * kbs / S);
+        }
+    }
+    return w;
 }
 
 // ----------------------------------------------------------------------------------------
@@ -445,10 +483,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_TMEM_SLOT);
-    int64_t total_tiles = p.total_tiles;
+    int64_t total_units = p.total_units;
     MoeTable mt{};
     if constexpr (Cfg::MOE) {
-        total_tiles = *reinterpret_cast<volatile int32_t*>(smem + Cfg::OFF_MOE_TOTAL);
+        total_units = *reinterpret_cast<volatile int32_t*>(smem + Cfg::OFF_MOE_TOTAL);
         mt.tile_pref = reinterpret_cast<const int32_t*>(smem + Cfg::OFF_MOE);
         mt.row_off = mt.tile_pref + (MOE_MAX_G + 1);
     }
@@ -464,8 +502,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             int64_t issued = 0;          // k-blocks whose loads this thread issued
             bool aborted = false;
             bool withhold = (p.withhold_kb >= 0) && blockIdx.x == 0;
-            for (int64_t t = unit; t < total_tiles && !aborted; t += num_units) {
-                g = find_problem<Cfg>(p, t, g, mt);
+            for (int64_t u = unit; u < total_units && !aborted; u += num_units) {
+                const Work w = work_of<Cfg>(p, u);
+                g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 if constexpr (Cfg::GROUPED) {
                     if (g != g_fenced) {
@@ -474,10 +513,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         g_fenced = g;
                     }
                 }
-                const TileCoord tc = tile_coord<Cfg>(p, t, g, rank, mt);
+                const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
                 const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // first B column this CTA loads
-                for (int kb = 0; kb < pr.k_blocks; ++kb) {
-                    if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, t, stage)) {
+                const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
+                for (int kb = w.kb0; kb < kb_end; ++kb) {
+                    if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, u, stage)) {
                         aborted = true;
                         break;
                     }
@@ -560,28 +600,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 if (lane == 0) ok = wait_bounded<CG, false>(bar, par, p, abort_addr, ROLE_MMA, tile, st) ? 1u : 0u;
                 return __shfl_sync(0xffffffffu, ok, 0) != 0;
             };
-            for (int64_t t = unit; t < total_tiles && !aborted; t += num_units) {
-                g = find_problem<Cfg>(p, t, g, mt);
+            for (int64_t u = unit; u < total_units && !aborted; u += num_units) {
+                const Work w = work_of<Cfg>(p, u);
+                g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 const uint32_t idesc = pr.idesc;
-                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, t, 16 + acc)) {
+                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, u, 16 + acc)) {
                     aborted = true;
                     break;
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const int k_blocks = pr.k_blocks;
-                const bool trace_tile = p.trace_tiles != nullptr && t < p.trace_tiles_cap;
-                for (int kb = 0; kb < k_blocks; ++kb) {
-                    if (!warp_wait(full_bar(stage), phase, t, stage)) {
+                const int kb_begin = w.kb0;
+                const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
+                const bool trace_unit = p.trace_tiles != nullptr && u < p.trace_tiles_cap;
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if (!warp_wait(full_bar(stage), phase, u, stage)) {
                         aborted = true;
                         break;
                     }
                     ptx::tc_fence_after_sync();
                     if (lane == 0) {
-                        if (kb == 0 && trace_tile) {
-                            p.trace_tiles[4 * t + 0] = blockIdx.x;
-                            p.trace_tiles[4 * t + 1] = ptx::globaltimer_ns();
+                        if (kb == kb_begin && trace_unit) {
+                            p.trace_tiles[4 * u + 0] = blockIdx.x;
+                            p.trace_tiles[4 * u + 1] = ptx::globaltimer_ns();
                         }
                         // stage s starts s * BYTES further on: add (s * BYTES) >> 4 to the start-address field
                         const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * Cfg::A_BYTES) >> 4);
@@ -593,7 +635,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
                             const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
                             ptx::mma_bf16<CG>(d_tmem, a_desc + a_off, b_desc + b_off, idesc,
-                                              (kb > 0 || kk > 0) ? 1u : 0u);
+                                              (kb > kb_begin || kk > 0) ? 1u : 0u);
                         }
                         if constexpr (CG == 2) ptx::mma_commit_pair(empty_bar(stage), 0x3);
                         else ptx::mma_commit(empty_bar(stage));
@@ -604,7 +646,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 }
                 if (aborted) break;
                 if (lane == 0) {
-                    if (k_blocks > 0) {
+                    if (kb_end > kb_begin) {
                         if constexpr (CG == 2) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
                         else ptx::mma_commit(tfull_bar(acc));
                     } else {
@@ -634,8 +676,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         uint32_t acc_phase = 0;
         int sbuf = 0;
         int g = 0, g_fenced = -1;
-        for (int64_t t = unit; t < total_tiles; t += num_units) {
-            g = find_problem<Cfg>(p, t, g, mt);
+        for (int64_t u = unit; u < total_units; u += num_units) {
+            const Work w = work_of<Cfg>(p, u);
+            g = find_problem<Cfg>(p, w.t, g, mt);
             const Problem& pr = problem_of<Cfg>(p, g);
             if constexpr (Cfg::GROUPED) {
                 if (lane == 0 && g != g_fenced) {
@@ -643,7 +686,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     g_fenced = g;
                 }
             }
-            const TileCoord tc = tile_coord<Cfg>(p, t, g, rank, mt);
+            const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
             const int row0 = tc.m0 + q * 32;
             int row_limit = pr.M;                     // rows of C this tile may write: [.., row_limit)
             if constexpr (Cfg::MOE) row_limit = static_cast<int>(min(static_cast<int64_t>(tc.row_end), p.moe_rows));
@@ -651,16 +694,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             // MoE: a slab that runs past its expert's rows is written row by row, without TMA
             const bool direct = Cfg::MOE && row0 + 32 > row_limit;
             const int epi = pr.epi;
-
+            const bool has_acc = (w.tail >= 0 ? w.kb1 - w.kb0 : pr.k_blocks) > 0;
 
             uint32_t ok = 1;
-            if (lane == 0) ok = wait_bounded<CG>(tfull_bar(acc), acc_phase, p, abort_addr, ROLE_EPILOGUE, t, 16 + acc) ? 1u : 0u;
+            if (lane == 0) ok = wait_bounded<CG>(tfull_bar(acc), acc_phase, p, abort_addr, ROLE_EPILOGUE, u, 16 + acc) ? 1u : 0u;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ptx::tc_fence_after_sync();
             __syncwarp();
-            const bool tracer = p.trace_tiles && lane == 0 && ew == 0 && leader && t < p.trace_tiles_cap;
-            if (tracer) p.trace_tiles[4 * t + 2] = ptx::globaltimer_ns();
+            const bool tracer = p.trace_tiles && lane == 0 && ew == 0 && leader && u < p.trace_tiles_cap;
+            if (tracer) p.trace_tiles[4 * u + 2] = ptx::globaltimer_ns();
 
             // RMS normalisation of A's row: one factor per accumulator row (this lane's row)
             float rs = 1.0f;
@@ -671,10 +714,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             constexpr int CHUNKS = BN / Cfg::CW;
-#pragma unroll 1
-            for (int c = 0; c < CHUNKS; ++c) {
-                float v[Cfg::CW];
-                if (pr.k_blocks > 0 && active) {
+
+            // accumulator columns [c * CW, (c + 1) * CW) of this lane's row; the last chunk
+            // hands the TMEM buffer back to the MMA issuer
+            auto read_chunk = [&](int c, float (&v)[Cfg::CW]) {
+                if (has_acc && active) {
                     uint32_t r[32];
 #pragma unroll
                     for (int h = 0; h < Cfg::CW / 32; ++h) {
@@ -688,7 +732,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     for (int i = 0; i < Cfg::CW; ++i) v[i] = 0.0f;
                 }
                 if (c == CHUNKS - 1) {
-                    // accumulator buffer fully read: hand it back to the MMA issuer
                     ptx::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
@@ -696,8 +739,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         else ptx::mbar_arrive(tempty_bar(acc));
                     }
                 }
+            };
+
+            // row scale, bias, GELU, rounding and the store of one chunk of final values
+            auto finish_chunk = [&](int c, float (&v)[Cfg::CW]) {
                 const int n_chunk = tc.n0 + c * Cfg::CW;
-                if (!active || n_chunk >= pr.N) continue;
+                if (!active || n_chunk >= pr.N) return;
                 if (pr.row_scale) {
 #pragma unroll
                     for (int i = 0; i < Cfg::CW; ++i) v[i] *= rs;
@@ -715,8 +762,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     if (n_chunk + Cfg::CW <= pr.N && (reinterpret_cast<uintptr_t>(bg) & 15u) == 0) {
 #pragma unroll
                         for (int j = 0; j < Cfg::CW / 8; ++j) {
-                            const uint4 w = __ldg(reinterpret_cast<const uint4*>(bg) + j);
-                            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                            const uint4 wv = __ldg(reinterpret_cast<const uint4*>(bg) + j);
+                            const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 v[8 * j + 2 * h] += widen(ws[h] & 0xffffu);
@@ -777,7 +824,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                  :: "r"(dst), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
                 }
-                if (direct) continue;
+                if (direct) return;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -792,8 +839,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     ptx::bulk_commit_group();
                 }
                 sbuf ^= 1;
+            };
+
+            bool whole = true;
+            if constexpr (!Cfg::GROUPED && !Cfg::MOE) whole = w.tail < 0;
+            if (whole) {
+#pragma unroll 1
+                for (int c = 0; c < CHUNKS; ++c) {
+                    float v[Cfg::CW];
+                    read_chunk(c, v);
+                    finish_chunk(c, v);
+                }
+            } else {
+                // Slice of a split tile: this warp's 32 x BN partial sums go to its own slab,
+                // float4 [column / 4][lane] so a warp's stores are 512 contiguous bytes.
+                const int S = p.sk_slices;
+                constexpr int64_t SLAB = 32 * BN;
+                auto slab = [&](int slice) {
+                    return reinterpret_cast<float4*>(
+                        p.sk_partial + ((static_cast<int64_t>(w.tail) * S + slice) * CG + rank) * 4 * SLAB + q * SLAB);
+                };
+                float4* mine = slab(w.slice);
+#pragma unroll 1
+                for (int c = 0; c < CHUNKS; ++c) {
+                    float v[Cfg::CW];
+                    read_chunk(c, v);
+                    if (active) {
+#pragma unroll
+                        for (int i = 0; i < Cfg::CW / 4; ++i)
+                            __stcg(mine + (c * (Cfg::CW / 4) + i) * 32 + lane,
+                                   make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                    }
+                }
+                if (active) {
+                    // publish: every lane's stores, then one arrival per warp
+                    __threadfence();
+                    __syncwarp();
+                    uint32_t last = 0;
+                    if (lane == 0) {
+                        ptx::grid_dependency_wait();   // the counters were zeroed by the kernel before this one
+                        const uint32_t idx = (static_cast<uint32_t>(w.tail) * CG + rank) * 4 + q;
+                        last = atomicAdd(p.sk_count + idx, 1u) == static_cast<uint32_t>(S - 1) ? 1u : 0u;
+                    }
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    if (last) {
+                        // the other slices' partials are visible: add all of them in slice order
+                        __threadfence();
+#pragma unroll 1
+                        for (int c = 0; c < CHUNKS; ++c) {
+                            float v[Cfg::CW];
+                            const float4* src0 = slab(0) + c * (Cfg::CW / 4) * 32 + lane;
+#pragma unroll
+                            for (int i = 0; i < Cfg::CW / 4; ++i) {
+                                const float4 x = __ldcg(src0 + i * 32);
+                                v[4 * i] = x.x;
+                                v[4 * i + 1] = x.y;
+                                v[4 * i + 2] = x.z;
+                                v[4 * i + 3] = x.w;
+                            }
+#pragma unroll 1
+                            for (int sl = 1; sl < S; ++sl) {
+                                const float4* src = slab(sl) + c * (Cfg::CW / 4) * 32 + lane;
+#pragma unroll
+                                for (int i = 0; i < Cfg::CW / 4; ++i) {
+                                    const float4 x = __ldcg(src + i * 32);
+                                    v[4 * i] += x.x;
+                                    v[4 * i + 1] += x.y;
+                                    v[4 * i + 2] += x.z;
+                                    v[4 * i + 3] += x.w;
+                                }
+                            }
+                            finish_chunk(c, v);
+                        }
+                    }
+                }
             }
-            if (tracer) p.trace_tiles[4 * t + 3] = ptx::globaltimer_ns();
+            if (tracer) p.trace_tiles[4 * u + 3] = ptx::globaltimer_ns();
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();

@@ -19,9 +19,12 @@ cudaError_t launch(const Params& p, int grid, cudaStream_t stream);
 template <class Cfg>
 cudaError_t resident_units(int* units);
 
-// r[i] = 1 / sqrt(mean_k A[i][k]^2 + eps) for a row-major bf16 A (tg_norm.cu).
+// tg_aux.cu.  r[i] = 1 / sqrt(mean_k A[i][k]^2 + eps) for a row-major bf16 A; the
+// first block also zeroes counters[0, n_counters) (split tiles of the GEMM that follows).
 cudaError_t launch_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps, float* r, int sms,
-                           cudaStream_t stream);
+                           cudaStream_t stream, uint32_t* counters = nullptr, int n_counters = 0);
+// counters[0, n) = 0, as a kernel the GEMM can follow as a programmatic dependent.
+cudaError_t launch_clear_counters(uint32_t* counters, int n, cudaStream_t stream);
 
 }  // namespace tg
 

@@ -33,8 +33,15 @@
  *    must be below 2^31.  Breaking these gives TG_ERR_UNSUPPORTED.
  *  - Degenerate sizes: M == 0 or N == 0 is a no-op returning TG_OK.  K == 0
  *    is the empty sum: C = epilogue(0), i.e. zeros, bias, or GELU(bias).
- *  - Results are deterministic: no split-K, no atomics; two identical calls
- *    write bitwise-identical C.
+ *  - Results are deterministic: two identical calls write bitwise-identical C.
+ *    Dense calls may compute the tiles of their last, partial wave as several
+ *    K-ranges on different SMs; those fp32 partials are added in a fixed
+ *    order (an atomic counter only picks which SM does the adding), so the
+ *    result does not depend on timing.  Set TG_SPLIT_TAIL=0 in the
+ *    environment to turn this off (one K-order per tile, as grouped calls).
+ *  - Dense calls with split tiles take a workspace from a library-owned
+ *    stream-ordered memory pool (at most (resident CTAs) x 128 KiB, released
+ *    on the stream after the launch).
  */
 #ifndef TG_H
 #define TG_H
@@ -287,9 +294,11 @@ tg_status tg_debug_withhold_stage(int64_t k_block);
  * by default, disarms itself after one launch).  Both buffers are DEVICE
  * memory owned by the caller; the kernel writes, with %globaltimer nanosecond
  * stamps:
- *   tile_records[4 t .. 4 t + 3] for global tile t < tile_capacity:
+ *   tile_records[4 w .. 4 w + 3] for work unit w < tile_capacity:
  *       {block index, first k-block ready for the MMA, accumulator complete,
- *        epilogue done} (tile order as scheduled: unit u runs tiles u, u + U, ...);
+ *        epilogue done}.  A work unit is a tile, or one K-range of a split
+ *       tile (dense calls split the tiles of their last, partial wave); CTA
+ *       (pair) i runs units i, i + U, i + 2U, ... for U resident CTAs (pairs);
  *   cta_records[2 b .. 2 b + 1] for block b < cta_capacity:
  *       {set-up done, teardown start}.
  * Capacities may be 0 to skip a buffer.  Grouped calls with several layout

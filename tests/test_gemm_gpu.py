@@ -269,7 +269,8 @@ def test_bcast_matches_materialised(U, repeat, N, K, epi):
     assert r["ok"] and r["max_tight"] < 4.0, r
 
 
-def test_bcast_equals_dense_on_materialised_bitwise():
+def test_bcast_equals_dense_on_materialised_bitwise(monkeypatch):
+    monkeypatch.setenv("TG_SPLIT_TAIL", "0")    # same summation order on both paths
     case = wl.dense_case("skinny_bcast")
     dense = run_dense(case)
     bc = tg.gemm_bcast(case.users.cuda(), case.b.cuda(), case.repeat, bias=case.bias.cuda(), epilogue="bias")
@@ -328,7 +329,8 @@ def test_grouped_ragged_with_empty_groups(epi, b_col, tile):
     _check_grouped(case, out, b_col=b_col)
 
 
-def test_grouped_single_group_matches_dense_bitwise(tile):
+def test_grouped_single_group_matches_dense_bitwise(tile, monkeypatch):
+    monkeypatch.setenv("TG_SPLIT_TAIL", "0")    # same summation order on both paths
     case = wl.dense_random(700, 392, 320, seed=22, dist="normal", epi="bias")
     a, b, bias = case.a.cuda(), case.b.cuda(), case.bias.cuda()
     dense = tg.gemm(a, b, bias=bias, epilogue="bias")
@@ -478,6 +480,60 @@ def test_timeline_trace_records_every_tile(tile):
     tg.gemm(a, b)
     _sync_ok()
     assert not tiles2.any()
+
+
+# ------------------------------------------------------------------------------------------ split tiles
+# The last, partial wave of a dense launch is cut along K: each of its tiles is
+# computed by several CTAs (pairs) at once and the last to finish adds the fp32
+# partials in slice order.  Shapes below: (a) more tiles than resident pairs, with
+# a small remainder (2304^2: 81 pair tiles on 76 pairs, 5 tiles split 4 ways);
+# (b) fewer tiles than CTAs (512^2 x 2048: 8 tiles split 8 ways); (c) a ragged
+# tail in M, N and K.
+
+SPLIT_SHAPES = [(2304, 2304, 1024), (512, 512, 2048), (1000, 776, 1480)]
+
+
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+@pytest.mark.parametrize("epi", ["none", "bias_gelu"])
+def test_split_tail_matches_oracle(M, N, K, epi):
+    case = wl.dense_random(M, N, K, seed=41, dist="normal", epi=epi)
+    c = run_dense(case)
+    _sync_ok()
+    check_dense(case, c)
+
+
+@pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
+def test_split_tail_deterministic_and_close_to_unsplit(c_dtype, monkeypatch):
+    case = wl.dense_random(2304, 2304, 1024, seed=42, dist="normal", c_dtype=c_dtype, epi="bias")
+    c1 = run_dense(case)
+    c2 = run_dense(case)
+    monkeypatch.setenv("TG_SPLIT_TAIL", "0")
+    c0 = run_dense(case)
+    _sync_ok()
+    assert torch.equal(c1, c2), "split tiles must not depend on which slice finishes last"
+    check_dense(case, c0)
+    check_dense(case, c1)
+
+
+def test_split_tail_integer_exact_bitwise():
+    # integer partial sums are exact in fp32, so the split result equals the exact one
+    for M, N, K in SPLIT_SHAPES:
+        case = wl.dense_random(M, N, K, seed=43, dist="int4", c_dtype="f32", **lds(M, N, K, False, False))
+        y, _ = oracle_dense(case)
+        c = run_dense(case)
+        _sync_ok()
+        assert np.array_equal(to_f64(c), y), (M, N, K)
+
+
+@pytest.mark.parametrize("tile_shape", TILES)
+def test_split_tail_every_variant(tile_shape, monkeypatch):
+    monkeypatch.setenv("TG_TILE", tile_shape)
+    for a_col, b_col in LAYOUTS:
+        case = wl.dense_random(640, 520, 1536, seed=44, dist="uniform", a_col_major=a_col, b_col_major=b_col,
+                               epi="bias", **lds(640, 520, 1536, a_col, b_col))
+        c = run_dense(case)
+        _sync_ok()
+        check_dense(case, c)
 
 
 # ------------------------------------------------------------------------------------------ full-size workloads
