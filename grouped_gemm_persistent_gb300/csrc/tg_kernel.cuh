@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "tg_ptx.cuh"
 
@@ -695,6 +696,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             const bool direct = Cfg::MOE && row0 + 32 > row_limit;
             const int epi = pr.epi;
             const bool has_acc = (w.tail >= 0 ? w.kb1 - w.kb0 : pr.k_blocks) > 0;
+            const bool f16b = (pr.flags & FLAG_BIAS_F16) != 0;
+
+            // The tile's bias, fetched before waiting for the accumulator so its latency
+            // is hidden: lane l holds the 16-bit values of columns [n0 + 8 l, n0 + 8 l + 8).
+            uint4 bias8 = make_uint4(0u, 0u, 0u, 0u);
+            if (epi != EPI_NONE && 8 * lane < BN) {
+                const int col = tc.n0 + 8 * lane;
+                const uint16_t* bg = reinterpret_cast<const uint16_t*>(pr.bias) + col +
+                                     (Cfg::MOE ? static_cast<int64_t>(tc.g) * pr.N : 0);
+                if (col + 8 <= pr.N && (reinterpret_cast<uintptr_t>(bg) & 15u) == 0) {
+                    bias8 = __ldg(reinterpret_cast<const uint4*>(bg));
+                } else {
+                    uint32_t h[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) h[i] = col + i < pr.N ? __ldg(bg + i) : 0u;
+                    bias8 = make_uint4(h[0] | h[1] << 16, h[2] | h[3] << 16, h[4] | h[5] << 16, h[6] | h[7] << 16);
+                }
+            }
 
             uint32_t ok = 1;
             if (lane == 0) ok = wait_bounded<CG>(tfull_bar(acc), acc_phase, p, abort_addr, ROLE_EPILOGUE, u, 16 + acc) ? 1u : 0u;
@@ -717,7 +736,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             // accumulator columns [c * CW, (c + 1) * CW) of this lane's row; the last chunk
             // hands the TMEM buffer back to the MMA issuer
-            auto read_chunk = [&](int c, float (&v)[Cfg::CW]) {
+            auto read_chunk = [&](int c, float (&v)[Cfg::CW], bool release) {
                 if (has_acc && active) {
                     uint32_t r[32];
 #pragma unroll
@@ -731,7 +750,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll
                     for (int i = 0; i < Cfg::CW; ++i) v[i] = 0.0f;
                 }
-                if (c == CHUNKS - 1) {
+                if (release && c == CHUNKS - 1) {
                     ptx::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
@@ -751,29 +770,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 }
 
                 if (epi != EPI_NONE) {
-                    // bias[n_chunk .. n_chunk + CW): the same values for every lane (broadcast loads)
-                    const uint16_t* bg = reinterpret_cast<const uint16_t*>(pr.bias) + n_chunk +
-                                         (Cfg::MOE ? static_cast<int64_t>(tc.g) * pr.N : 0);
-                    const bool f16b = (pr.flags & FLAG_BIAS_F16) != 0;
-                    auto widen = [&](uint32_t h) {
-                        return f16b ? __half2float(__ushort_as_half(static_cast<unsigned short>(h)))
-                                    : __uint_as_float(h << 16);
-                    };
-                    if (n_chunk + Cfg::CW <= pr.N && (reinterpret_cast<uintptr_t>(bg) & 15u) == 0) {
+                    // bias of columns [n_chunk, n_chunk + CW): 8 columns from each of CW / 8 lanes
+                    auto add_bias = [&](auto f16_tag) {
+                        constexpr bool F16 = decltype(f16_tag)::value;
+                        auto widen = [](uint32_t h) {
+                            if constexpr (F16) return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+                            else return __uint_as_float(h << 16);
+                        };
 #pragma unroll
                         for (int j = 0; j < Cfg::CW / 8; ++j) {
-                            const uint4 wv = __ldg(reinterpret_cast<const uint4*>(bg) + j);
-                            const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+                            const int src = c * (Cfg::CW / 8) + j;
+                            const uint32_t ws[4] = {__shfl_sync(0xffffffffu, bias8.x, src),
+                                                    __shfl_sync(0xffffffffu, bias8.y, src),
+                                                    __shfl_sync(0xffffffffu, bias8.z, src),
+                                                    __shfl_sync(0xffffffffu, bias8.w, src)};
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {
                                 v[8 * j + 2 * h] += widen(ws[h] & 0xffffu);
                                 v[8 * j + 2 * h + 1] += widen(ws[h] >> 16);
                             }
                         }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < Cfg::CW; ++i) v[i] += (n_chunk + i < pr.N) ? widen(__ldg(bg + i)) : 0.0f;
-                    }
+                    };
+                    if (f16b) add_bias(std::true_type{});
+                    else add_bias(std::false_type{});
                     if (epi == EPI_BIAS_GELU) {
 #pragma unroll
                         for (int i = 0; i < Cfg::CW; ++i) v[i] = gelu_tanh_f32(v[i]);
@@ -847,7 +866,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll 1
                 for (int c = 0; c < CHUNKS; ++c) {
                     float v[Cfg::CW];
-                    read_chunk(c, v);
+                    read_chunk(c, v, true);
                     finish_chunk(c, v);
                 }
             } else {
@@ -860,10 +879,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         p.sk_partial + ((static_cast<int64_t>(w.tail) * S + slice) * CG + rank) * 4 * SLAB + q * SLAB);
                 };
                 float4* mine = slab(w.slice);
+                // the accumulator stays in TMEM until it is known whether this slice adds up
 #pragma unroll 1
                 for (int c = 0; c < CHUNKS; ++c) {
                     float v[Cfg::CW];
-                    read_chunk(c, v);
+                    read_chunk(c, v, false);
                     if (active) {
 #pragma unroll
                         for (int i = 0; i < Cfg::CW / 4; ++i)
@@ -871,23 +891,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
                     }
                 }
+                uint32_t last = 0;
                 if (active) {
                     // publish: every lane's stores, then one arrival per warp
                     __threadfence();
                     __syncwarp();
-                    uint32_t last = 0;
                     if (lane == 0) {
                         ptx::grid_dependency_wait();   // the counters were zeroed by the kernel before this one
                         const uint32_t idx = (static_cast<uint32_t>(w.tail) * CG + rank) * 4 + q;
                         last = atomicAdd(p.sk_count + idx, 1u) == static_cast<uint32_t>(S - 1) ? 1u : 0u;
                     }
                     last = __shfl_sync(0xffffffffu, last, 0);
-                    if (last) {
-                        // the other slices' partials are visible: add all of them in slice order
-                        __threadfence();
+                }
+                if (last) {
+                    // the other slices' partials are visible: add all S in slice order, this
+                    // slice's own from TMEM (the same values it stored)
+                    __threadfence();
 #pragma unroll 1
-                        for (int c = 0; c < CHUNKS; ++c) {
-                            float v[Cfg::CW];
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        float v[Cfg::CW];
+                        if (w.slice == 0) {
+                            read_chunk(c, v, c == CHUNKS - 1);
+                        } else {
                             const float4* src0 = slab(0) + c * (Cfg::CW / 4) * 32 + lane;
 #pragma unroll
                             for (int i = 0; i < Cfg::CW / 4; ++i) {
@@ -897,20 +922,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                                 v[4 * i + 2] = x.z;
                                 v[4 * i + 3] = x.w;
                             }
+                        }
 #pragma unroll 1
-                            for (int sl = 1; sl < S; ++sl) {
+                        for (int sl = 1; sl < S; ++sl) {
+                            float x[Cfg::CW];
+                            if (sl == w.slice) {
+                                read_chunk(c, x, c == CHUNKS - 1);
+                            } else {
                                 const float4* src = slab(sl) + c * (Cfg::CW / 4) * 32 + lane;
 #pragma unroll
                                 for (int i = 0; i < Cfg::CW / 4; ++i) {
-                                    const float4 x = __ldcg(src + i * 32);
-                                    v[4 * i] += x.x;
-                                    v[4 * i + 1] += x.y;
-                                    v[4 * i + 2] += x.z;
-                                    v[4 * i + 3] += x.w;
+                                    const float4 y = __ldcg(src + i * 32);
+                                    x[4 * i] = y.x;
+                                    x[4 * i + 1] = y.y;
+                                    x[4 * i + 2] = y.z;
+                                    x[4 * i + 3] = y.w;
                                 }
                             }
-                            finish_chunk(c, v);
+#pragma unroll
+                            for (int i = 0; i < Cfg::CW; ++i) v[i] += x[i];
                         }
+                        finish_chunk(c, v);
+                    }
+                } else {
+                    // not the last slice (or no rows here): hand the accumulator back
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (CG == 2 && !leader) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
+                        else ptx::mbar_arrive(tempty_bar(acc));
                     }
                 }
             }
