@@ -50,6 +50,7 @@ constexpr int UMMA_K = 16;           // K per tcgen05.mma.kind::f16
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;         // warps 2..5 drain TMEM; warp w reads lanes 32*(w%4)..+31
 constexpr int NUM_EPI_WARPS = 4;
+constexpr int FIX_BUFS = 4;    // chunks in flight per warp while adding up a split tile
 constexpr int C_STAGE_BYTES = 32 * 128;   // per-warp store staging buffer: 32 rows x 128 bytes
 constexpr int SMEM_LIMIT = 232448;        // max dynamic shared memory per CTA on sm_100 family
 constexpr int MOE_MAX_G = 190;            // experts per call of the device-counts MoE form (table in shared memory)
@@ -179,6 +180,8 @@ struct Config {
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
     static_assert(BN_CTA % 64 == 0, "MN-major B is loaded in 64-column boxes");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
+    static_assert(NUM_EPI_WARPS * FIX_BUFS * 32 * CW * 4 <= STAGES * STAGE_BYTES,
+                  "split-tile staging must fit in the operand ring");
 };
 
 // ----------------------------------------------------------------------------------------
@@ -904,46 +907,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     last = __shfl_sync(0xffffffffu, last, 0);
                 }
                 if (last) {
-                    // the other slices' partials are visible: add all S in slice order, this
-                    // slice's own from TMEM (the same values it stored)
+                    // The other slices' partials are visible.  Add all S in slice order, this
+                    // slice's own from TMEM (the same values it stored).  The others stream
+                    // through this warp's share of the operand ring - idle now, because a
+                    // slice is always its CTA's last work unit - with cp.async, FIX_BUFS
+                    // chunks in flight; each lane copies and reads back only its own float4s.
                     __threadfence();
+                    constexpr int CH_BYTES = 32 * Cfg::CW * 4;
+                    const uint32_t region = sA + static_cast<uint32_t>(q) * FIX_BUFS * CH_BYTES;
+                    const int items = CHUNKS * (S - 1);      // (chunk, other slice), chunk-major
+                    auto issue = [&](int k) {
+                        if (k < items) {
+                            const int c = k / (S - 1), j = k % (S - 1);
+                            const float4* src = slab(j < w.slice ? j : j + 1) + c * (Cfg::CW / 4) * 32 + lane;
+                            const uint32_t dst = region + static_cast<uint32_t>(k % FIX_BUFS) * CH_BYTES + lane * 16u;
+#pragma unroll
+                            for (int i = 0; i < Cfg::CW / 4; ++i) ptx::cp_async_16(dst + i * 512u, src + i * 32);
+                        }
+                        ptx::cp_async_commit();              // empty groups keep the count uniform
+                    };
+#pragma unroll 1
+                    for (int k = 0; k < FIX_BUFS - 1; ++k) issue(k);
+                    int k = 0;
 #pragma unroll 1
                     for (int c = 0; c < CHUNKS; ++c) {
                         float v[Cfg::CW];
-                        if (w.slice == 0) {
-                            read_chunk(c, v, c == CHUNKS - 1);
-                        } else {
-                            const float4* src0 = slab(0) + c * (Cfg::CW / 4) * 32 + lane;
-#pragma unroll
-                            for (int i = 0; i < Cfg::CW / 4; ++i) {
-                                const float4 x = __ldcg(src0 + i * 32);
-                                v[4 * i] = x.x;
-                                v[4 * i + 1] = x.y;
-                                v[4 * i + 2] = x.z;
-                                v[4 * i + 3] = x.w;
-                            }
-                        }
 #pragma unroll 1
-                        for (int sl = 1; sl < S; ++sl) {
+                        for (int sl = 0; sl < S; ++sl) {
                             float x[Cfg::CW];
                             if (sl == w.slice) {
                                 read_chunk(c, x, c == CHUNKS - 1);
                             } else {
-                                const float4* src = slab(sl) + c * (Cfg::CW / 4) * 32 + lane;
+                                ptx::cp_async_wait<FIX_BUFS - 2>();   // item k has landed
+                                const uint32_t buf = region + static_cast<uint32_t>(k % FIX_BUFS) * CH_BYTES + lane * 16u;
 #pragma unroll
                                 for (int i = 0; i < Cfg::CW / 4; ++i) {
-                                    const float4 y = __ldcg(src + i * 32);
+                                    const float4 y = ptx::ld_shared_f4(buf + i * 512u);
                                     x[4 * i] = y.x;
                                     x[4 * i + 1] = y.y;
                                     x[4 * i + 2] = y.z;
                                     x[4 * i + 3] = y.w;
                                 }
+                                issue(k + FIX_BUFS - 1);          // into the buffer of item k - 1
+                                ++k;
                             }
+                            if (sl == 0) {
 #pragma unroll
-                            for (int i = 0; i < Cfg::CW; ++i) v[i] += x[i];
+                                for (int i = 0; i < Cfg::CW; ++i) v[i] = x[i];
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < Cfg::CW; ++i) v[i] += x[i];
+                            }
                         }
                         finish_chunk(c, v);
                     }
+                    ptx::cp_async_wait<0>();
                 } else {
                     // not the last slice (or no rows here): hand the accumulator back
                     ptx::tc_fence_before_sync();

@@ -290,6 +290,21 @@ __host__ __device__ constexpr uint32_t idesc_f32_acc(uint32_t M, uint32_t N, boo
            ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// cp.async: 16-byte asynchronous copies global -> shared (L2 only), per-thread groups
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start once every block of the kernel before it has called
 // launch_dependents (or exited); wait returns when that kernel has completed and
