@@ -370,14 +370,6 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     return TG_OK;
 }
 
-// k-blocks between a load and the L2 prefetch issued with it (TG_PREFETCH_KB; 0 = off)
-int prefetch_distance() {
-    const char* env = std::getenv("TG_PREFETCH_KB");
-    if (!env) return 0;
-    const int v = std::atoi(env);
-    return v < 0 ? 0 : (v > 64 ? 64 : v);
-}
-
 void base_params(Params* p, DeviceState* d) {
     p->err = d->err;
     p->wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
@@ -388,7 +380,6 @@ void base_params(Params* p, DeviceState* d) {
     p->trace_ctas = t_trace.ctas;
     p->trace_ctas_cap = t_trace.ctas_cap;
     t_trace = TraceArm{};
-    p->prefetch_kb = prefetch_distance();
 }
 
 tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t stream) {

@@ -134,9 +134,6 @@ struct Params {
     int32_t sk_slices;          // 0: no split
     float* sk_partial;          // [sk_tiles][sk_slices][CTA_GROUP][4 warps][BN/4][32 lanes][4]
     uint32_t* sk_count;         // [sk_tiles][CTA_GROUP][4 warps]
-    // The producer asks L2 for the operands of k-block kb + prefetch_kb (of this work
-    // unit or the next one) when it loads k-block kb; 0 turns this off.
-    int32_t prefetch_kb;
 };
 
 // MODE: 0 dense (tensor maps in parameter space), 1 grouped (problem table in
@@ -523,48 +520,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
                 const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // first B column this CTA loads
                 const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
-                // L2 prefetch: the operands of one k-block of (problem, tile)
-                auto prefetch = [&](const Problem& q, const TileCoord& c, int kb) {
-                    const int k0 = kb * BK;
-                    const int n0 = c.n0 + static_cast<int>(rank) * Cfg::BN_CTA;
-                    if constexpr (Cfg::A_MN) {
-                        ptx::tma_prefetch_2d(&q.tma_a, c.m0, k0);
-                        ptx::tma_prefetch_2d(&q.tma_a, c.m0 + 64, k0);
-                    } else {
-                        ptx::tma_prefetch_2d(&q.tma_a, k0, c.m0);
-                    }
-                    if constexpr (Cfg::MOE) {
-                        if constexpr (Cfg::B_MN) {
-#pragma unroll
-                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j) ptx::tma_prefetch_3d(&q.tma_b, n0 + j * 64, k0, c.g);
-                        } else {
-                            ptx::tma_prefetch_3d(&q.tma_b, k0, n0, c.g);
-                        }
-                    } else if constexpr (Cfg::B_MN) {
-#pragma unroll
-                        for (int j = 0; j < Cfg::BN_CTA / 64; ++j) ptx::tma_prefetch_2d(&q.tma_b, n0 + j * 64, k0);
-                    } else {
-                        ptx::tma_prefetch_2d(&q.tma_b, k0, n0);
-                    }
-                };
-                // the next work unit of this CTA, for prefetches that run past this one
-                const int pf = p.prefetch_kb;
-                int g_next = g, nkb0 = 0, nkb_end = 0;
-                TileCoord tc_next = tc;
-                if (pf > 0 && u + num_units < total_units) {
-                    const Work wn = work_of<Cfg>(p, u + num_units);
-                    g_next = find_problem<Cfg>(p, wn.t, g, mt);
-                    const Problem& pn = problem_of<Cfg>(p, g_next);
-                    if constexpr (Cfg::GROUPED) {
-                        if (g_next != g) {
-                            ptx::fence_tensormap_acquire(&pn.tma_a);
-                            ptx::fence_tensormap_acquire(&pn.tma_b);
-                        }
-                    }
-                    tc_next = tile_coord<Cfg>(p, wn.t, g_next, rank, mt);
-                    nkb0 = wn.kb0;
-                    nkb_end = wn.tail >= 0 ? wn.kb1 : pn.k_blocks;
-                }
                 for (int kb = w.kb0; kb < kb_end; ++kb) {
                     if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, u, stage)) {
                         aborted = true;
@@ -605,14 +560,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             load(b_dst, &pr.tma_b, k0, nb0);
                         }
                         ++issued;
-                        if (pf > 0) {
-                            const int kp = kb + pf;
-                            if (kp < kb_end) {
-                                prefetch(pr, tc, kp);
-                            } else if (nkb0 + (kp - kb_end) < nkb_end) {
-                                prefetch(problem_of<Cfg>(p, g_next), tc_next, nkb0 + (kp - kb_end));
-                            }
-                        }
                     }
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }

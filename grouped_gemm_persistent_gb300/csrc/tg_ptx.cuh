@@ -133,16 +133,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(cluster_bar) : "memory");
 }
 
-// L2 prefetch of the box a tiled load with the same map and coordinates would read.
-__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" :: "l"(tmap), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" :: "l"(tmap), "r"(x), "r"(y),
-                 "r"(z) : "memory");
-}
-
 // 3-D tiled load global -> own shared memory, completion on an mbarrier of this CTA.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                                             uint32_t bar) {
