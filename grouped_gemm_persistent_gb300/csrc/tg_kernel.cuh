@@ -584,10 +584,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
-        // One thread runs the loop.  The tensor pipe needs 4 x 128 cycles per k-block;
-        // warp-wide votes and syncs per k-block cost more than the issue itself and
-        // kept the pipe waiting, so lanes 1-31 go straight to the teardown.
-        if (leader && lane == 0) {
+        // The whole warp runs the loop, converged; lane 0 issues the MMAs and commits.
+        if (leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -595,24 +593,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             int g = 0;
             bool aborted = false;
             bool any_mma = false;
-            // shared-memory descriptors of stage 0 (A and B); stage s starts s * BYTES further
-            // on, i.e. (s * BYTES) >> 4 further in the start-address field
+            // shared-memory descriptors of stage 0 (A and B)
             const uint64_t a_desc0 = Cfg::A_MN ? ptx::smem_desc_sw128(sA, 8192, 1024) : ptx::smem_desc_sw128(sA, 16, 1024);
             const uint64_t b_desc0 = Cfg::B_MN ? ptx::smem_desc_sw128(sB, 8192, 1024) : ptx::smem_desc_sw128(sB, 16, 1024);
-            // K-major: the next 16 K elements are 32 bytes further along the swizzled row;
-            // MN-major: 16 rows (2048 bytes) further down
-            constexpr uint64_t A_STEP = Cfg::A_MN ? (2048u >> 4) : (32u >> 4);
-            constexpr uint64_t B_STEP = Cfg::B_MN ? (2048u >> 4) : (32u >> 4);
-            auto wait = [&](uint32_t bar, uint32_t par, int64_t tile, uint32_t st) -> bool {
-                if (ptx::mbar_try_wait(bar, par)) return true;
-                return wait_bounded<CG, false>(bar, par, p, abort_addr, ROLE_MMA, tile, st);
+            // Warp-uniform bounded wait: every lane polls once; if the phase is not yet
+            // complete, lane 0 runs the bounded wait and tells the others how it ended.
+            auto warp_wait = [&](uint32_t bar, uint32_t par, int64_t tile, uint32_t st) -> bool {
+                if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, par))) return true;
+                uint32_t ok = 1;
+                if (lane == 0) ok = wait_bounded<CG, false>(bar, par, p, abort_addr, ROLE_MMA, tile, st) ? 1u : 0u;
+                return __shfl_sync(0xffffffffu, ok, 0) != 0;
             };
             for (int64_t u = unit; u < total_units && !aborted; u += num_units) {
                 const Work w = work_of<Cfg>(p, u);
                 g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 const uint32_t idesc = pr.idesc;
-                if (!wait(tempty_bar(acc), acc_phase ^ 1u, u, 16 + acc)) {
+                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, u, 16 + acc)) {
                     aborted = true;
                     break;
                 }
@@ -620,46 +617,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 const int kb_begin = w.kb0;
                 const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
-                if (p.trace_tiles != nullptr && u < p.trace_tiles_cap && kb_end > kb_begin)
-                    p.trace_tiles[4 * u + 0] = blockIdx.x;
-                uint32_t accumulate = 0u;
+                const bool trace_unit = p.trace_tiles != nullptr && u < p.trace_tiles_cap;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!wait(full_bar(stage), phase, u, stage)) {
+                    if (!warp_wait(full_bar(stage), phase, u, stage)) {
                         aborted = true;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    if (kb == kb_begin && p.trace_tiles != nullptr && u < p.trace_tiles_cap)
-                        p.trace_tiles[4 * u + 1] = ptx::globaltimer_ns();
-                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * Cfg::A_BYTES) >> 4);
-                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_BYTES) >> 4);
+                    if (lane == 0) {
+                        if (kb == kb_begin && trace_unit) {
+                            p.trace_tiles[4 * u + 0] = blockIdx.x;
+                            p.trace_tiles[4 * u + 1] = ptx::globaltimer_ns();
+                        }
+                        // stage s starts s * BYTES further on: add (s * BYTES) >> 4 to the start-address field
+                        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * Cfg::A_BYTES) >> 4);
+                        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_BYTES) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        ptx::mma_bf16<CG>(d_tmem, a_desc + kk * A_STEP, b_desc + kk * B_STEP, idesc, accumulate);
-                        accumulate = 1u;
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            // K-major: the next 16 K elements are 32 bytes further along the
+                            // swizzled row; MN-major: 16 rows (2048 bytes) further down.
+                            const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
+                            const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
+                            ptx::mma_bf16<CG>(d_tmem, a_desc + a_off, b_desc + b_off, idesc,
+                                              (kb > kb_begin || kk > 0) ? 1u : 0u);
+                        }
+                        if constexpr (CG == 2) ptx::mma_commit_pair(empty_bar(stage), 0x3);
+                        else ptx::mma_commit(empty_bar(stage));
                     }
-                    if constexpr (CG == 2) ptx::mma_commit_pair(empty_bar(stage), 0x3);
-                    else ptx::mma_commit(empty_bar(stage));
+                    __syncwarp();
                     any_mma = true;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (aborted) break;
-                if (kb_end > kb_begin) {
-                    if constexpr (CG == 2) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
-                    else ptx::mma_commit(tfull_bar(acc));
-                } else {
-                    // K == 0: nothing to accumulate; the epilogue writes epilogue(0).
-                    ptx::mbar_arrive(tfull_bar(acc));
-                    if constexpr (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa(tfull_bar(acc), 1));
+                if (lane == 0) {
+                    if (kb_end > kb_begin) {
+                        if constexpr (CG == 2) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
+                        else ptx::mma_commit(tfull_bar(acc));
+                    } else {
+                        // K == 0: nothing to accumulate; the epilogue writes epilogue(0).
+                        ptx::mbar_arrive(tfull_bar(acc));
+                        if constexpr (CG == 2) ptx::mbar_arrive_cluster(ptx::mapa(tfull_bar(acc), 1));
+                    }
                 }
+                __syncwarp();
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
-            if (aborted && any_mma) {
+            if (aborted && any_mma && lane == 0) {
                 // Drain: one more commit completes when every MMA issued so far has.
                 if constexpr (CG == 2) ptx::mma_commit_pair(drain_bar, 0x1);
                 else ptx::mma_commit(drain_bar);
                 if (!wait_quiet(drain_bar, 0, p.wait_budget_ns)) report_timeout(p, ROLE_DRAIN, -1, 0, p.wait_budget_ns);
             }
+            __syncwarp();
         }
     } else {
         // ================================ epilogue ================================
