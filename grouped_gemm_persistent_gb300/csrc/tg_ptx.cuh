@@ -238,6 +238,40 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  :: "r"(bar));
 }
 
+// The same two, executed by every lane of a converged warp with only the lanes that have
+// `issue` set performing them (a guard predicate instead of a branch): the issuing warp
+// never diverges, and the per-k-block cost of reconverging is gone.
+template <int CTA_GROUP>
+__device__ __forceinline__ void mma_bf16_guarded(bool issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    if constexpr (CTA_GROUP == 1)
+        asm volatile(
+            "{\n\t.reg .pred p, g;\n\t"
+            "setp.ne.u32 p, %4, 0;\n\t"
+            "setp.ne.u32 g, %5, 0;\n\t"
+            "@g tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(issue)));
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, g;\n\t"
+            "setp.ne.u32 p, %4, 0;\n\t"
+            "setp.ne.u32 g, %5, 0;\n\t"
+            "@g tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(static_cast<uint32_t>(issue)));
+}
+
+template <int CTA_GROUP>
+__device__ __forceinline__ void mma_commit_guarded(bool issue, uint32_t bar) {
+    if constexpr (CTA_GROUP == 1)
+        asm volatile("{\n\t.reg .pred g;\n\tsetp.ne.u32 g, %1, 0;\n\t"
+                     "@g tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+                     :: "r"(bar), "r"(static_cast<uint32_t>(issue)));
+    else
+        asm volatile("{\n\t.reg .pred g;\n\tsetp.ne.u32 g, %1, 0;\n\t"
+                     "@g tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %2;\n\t}"
+                     :: "r"(bar), "r"(static_cast<uint32_t>(issue)), "h"(static_cast<uint16_t>(0x3)));
+}
+
 // Same for a CTA pair: arrive on the barrier at offset `bar` in every CTA named by `cta_mask`.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
