@@ -193,6 +193,12 @@ struct TileCoord {
     int n0;       // first column of the tile
     int r;        // replica index (broadcast form), else 0
     int row_end;  // MoE: first row past this expert's rows; otherwise INT32_MAX
+    // Half tile (grouped and MoE pairs): a problem's last M-tile with at most 128 rows
+    // left is computed by 256 x 16 x 128-row MMAs (M = 128 for the pair), which take
+    // half the time of M = 256.  Each CTA then holds 64 rows; its accumulator keeps
+    // columns [0, BN/2) in TMEM lanes 0-63 and [BN/2, BN) in lanes 64-127, both in
+    // TMEM columns [0, BN/2).
+    bool half;
 };
 
 // Device-counts MoE schedule, built in shared memory by every CTA at start:
@@ -247,7 +253,12 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     const int nb = n_first + (r - mb * width);
     TileCoord c;
     c.g = g;
-    c.m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * BM;
+    c.half = false;
+    if constexpr (Cfg::CTA_GROUP == 2 && (Cfg::GROUPED || Cfg::MOE)) {
+        const int rows_left = (Cfg::MOE ? mt.row_off[g + 1] - mt.row_off[g] : pr.M) - mb * Cfg::TILE_M;
+        c.half = rows_left <= BM;
+    }
+    c.m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * (c.half ? BM / 2 : BM);
     c.n0 = nb * Cfg::BN;
     c.r = replica;
     c.row_end = INT32_MAX;
@@ -608,7 +619,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const Work w = work_of<Cfg>(p, u);
                 g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
-                const uint32_t idesc = pr.idesc;
+                // half tiles: M = 128 for the pair (bits 24-28 of the instruction descriptor hold M >> 4)
+                const bool half = tile_coord<Cfg>(p, w.t, g, rank, mt).half;
+                const uint32_t idesc = half ? (pr.idesc & ~(0x1Fu << 24)) | ((128u >> 4) << 24) : pr.idesc;
                 if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, u, 16 + acc)) {
                     aborted = true;
                     break;
@@ -690,7 +703,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 }
             }
             const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
-            const int row0 = tc.m0 + q * 32;
+            // half tiles: warps q and q + 2 share rows (q % 2) * 32 .. + 32 of this CTA's 64,
+            // warp q / 2 == 1 taking columns [BN/2, BN)
+            const int row0 = tc.m0 + (tc.half ? (q % 2) * 32 : q * 32);
+            const int col_base = tc.half ? (q / 2) * (BN / 2) : 0;
             int row_limit = pr.M;                     // rows of C this tile may write: [.., row_limit)
             if constexpr (Cfg::MOE) row_limit = static_cast<int>(min(static_cast<int64_t>(tc.row_end), p.moe_rows));
             const bool active = row0 < row_limit;
@@ -735,6 +751,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             constexpr int CHUNKS = BN / Cfg::CW;
+            const int n_chunks = tc.half ? CHUNKS / 2 : CHUNKS;
 
             // accumulator columns [c * CW, (c + 1) * CW) of this lane's row; the last chunk
             // hands the TMEM buffer back to the MMA issuer
@@ -752,7 +769,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 #pragma unroll
                     for (int i = 0; i < Cfg::CW; ++i) v[i] = 0.0f;
                 }
-                if (release && c == CHUNKS - 1) {
+                if (release && c == n_chunks - 1) {
                     ptx::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
@@ -764,7 +781,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             // row scale, bias, GELU, rounding and the store of one chunk of final values
             auto finish_chunk = [&](int c, float (&v)[Cfg::CW]) {
-                const int n_chunk = tc.n0 + c * Cfg::CW;
+                const int n_chunk = tc.n0 + col_base + c * Cfg::CW;
                 if (!active || n_chunk >= pr.N) return;
                 if (pr.row_scale) {
 #pragma unroll
@@ -781,7 +798,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         };
 #pragma unroll
                         for (int j = 0; j < Cfg::CW / 8; ++j) {
-                            const int src = c * (Cfg::CW / 8) + j;
+                            const int src = (col_base + c * Cfg::CW) / 8 + j;
                             const uint32_t ws[4] = {__shfl_sync(0xffffffffu, bias8.x, src),
                                                     __shfl_sync(0xffffffffu, bias8.y, src),
                                                     __shfl_sync(0xffffffffu, bias8.z, src),
@@ -866,7 +883,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             if constexpr (!Cfg::GROUPED && !Cfg::MOE) whole = w.tail < 0;
             if (whole) {
 #pragma unroll 1
-                for (int c = 0; c < CHUNKS; ++c) {
+                for (int c = 0; c < n_chunks; ++c) {
                     float v[Cfg::CW];
                     read_chunk(c, v, true);
                     finish_chunk(c, v);

@@ -365,6 +365,56 @@ def test_grouped_mixed_layouts_and_dtypes(tile):
         assert r["ok"] and r["max_tight"] < 4.0, r
 
 
+# Half tiles: with CTA pairs, a problem's last M-tile with at most 128 rows left runs
+# as M = 128 MMAs (64 rows per CTA, accumulator columns split over the TMEM lane
+# halves).  Row counts around every boundary, both tile widths, all layouts.
+HALF_COUNTS = [1, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257, 300, 384, 385, 640]
+
+
+@pytest.mark.parametrize("tile_shape", ["2x256", "2x128"])
+@pytest.mark.parametrize("a_col,b_col", LAYOUTS)
+@pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
+def test_grouped_half_tiles(tile_shape, a_col, b_col, c_dtype, monkeypatch):
+    monkeypatch.setenv("TG_TILE", tile_shape)
+    gen = torch.Generator().manual_seed(61)
+    N, K = 264, 136
+    probs, refs, keep = [], [], []
+    for M in HALF_COUNTS:
+        a = (torch.randn((K, M) if a_col else (M, K), generator=gen) / 8).to(torch.bfloat16)
+        b = (torch.randn((N, K) if b_col else (K, N), generator=gen) / 8).to(torch.bfloat16)
+        bias = (torch.randn((N,), generator=gen) / 10).to(torch.bfloat16)
+        if a_col:
+            a = torch.nn.functional.pad(a, (0, (-M) % 8))[:, :M]      # column stride a multiple of 8
+        da, db, dbias = to_device(a), b.cuda(), bias.cuda()
+        out = torch.full((M, N), float("nan"), dtype=torch.float32 if c_dtype == "f32" else torch.bfloat16,
+                         device="cuda")
+        keep += [da, db, dbias, out]
+        probs.append(tg.make_problem(da.t() if a_col else da, db.t() if b_col else db, out, bias=dbias,
+                                     epilogue="bias_gelu"))
+        refs.append((a, b, bias, out))
+    tg.grouped_gemm_table(probs)
+    _sync_ok()
+    for a, b, bias, out in refs:
+        y, s = oracle.gemm(wl.bf16_bits(a.contiguous()), wl.bf16_bits(b), a_col_major=a_col, b_col_major=b_col,
+                           bias=wl.bf16_bits(bias), epi="bias_gelu")
+        r = oracle.compare(to_f64(out), y, s, np.abs(bias.double().numpy()))
+        assert r["ok"] and r["max_tight"] < 4.0, (out.shape, r)
+
+
+@pytest.mark.parametrize("tile_shape", ["2x256", "2x128"])
+def test_moe_half_tiles_device_counts(tile_shape, monkeypatch):
+    monkeypatch.setenv("TG_TILE", tile_shape)
+    counts = [129, 1, 128, 0, 64, 257, 385, 127]
+    case, a, b, bias, T = _moe_case(counts, 200, 136, 62, epi="bias_gelu", extra_rows=40)
+    out = torch.full((T, 200), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tg.moe_gemm_device(a, b, torch.tensor(counts, dtype=torch.int32, device="cuda"), out, bias=bias,
+                       epilogue="bias_gelu")
+    _sync_ok()
+    total = int(np.sum(counts))
+    assert torch.isnan(out[total:].float()).all(), "rows past the counts were written"
+    _check_grouped(case, out[:total])
+
+
 # ------------------------------------------------------------------------------------------ MoE, device counts
 
 def _moe_case(counts, N, K, seed, epi="none", b_col=False, extra_rows=0):
