@@ -557,15 +557,27 @@ struct SplitPlan {
     int64_t first = 0;   // first split tile
     int tiles = 0;       // R
     int slices = 0;      // S (0: no split)
+    bool nsplit = false; // column halves instead of K-ranges
 };
 
-SplitPlan plan_split(int64_t tiles, int units, int k_blocks) {
+// The last wave's R tiles: cut into two column halves when they then fit (2R units)
+// - a 256-wide tile's N = 128 MMAs take half the time and need no partial sums -
+// else into S K-ranges.
+SplitPlan plan_split(int64_t tiles, int units, int k_blocks, int bn) {
     SplitPlan sp;
     const char* env = std::getenv("TG_SPLIT_TAIL");
     if (env && env[0] == '0') return sp;
-    if (units <= 0 || k_blocks < 2 * kMinSliceKb) return sp;
+    if (units <= 0) return sp;
     const int64_t R = tiles % units;
     if (R == 0) return sp;
+    if (bn == 256 && tiles > units && 2 * R <= units && !(env && env[0] == 'k')) {
+        sp.first = tiles - R;
+        sp.tiles = static_cast<int>(R);
+        sp.slices = 2;
+        sp.nsplit = true;
+        return sp;
+    }
+    if (k_blocks < 2 * kMinSliceKb) return sp;
     int64_t S = units / R;
     if (S > k_blocks / kMinSliceKb) S = k_blocks / kMinSliceKb;
     if (S > kMaxSlices) S = kMaxSlices;
@@ -607,10 +619,16 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
     base_params(&p, d);
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const SplitPlan sp = plan_split(tiles, units, p.dense.k_blocks);
+    const SplitPlan sp = plan_split(tiles, units, p.dense.k_blocks, v.bn);
     void* ws = nullptr;
     int n_counters = 0;
-    if (sp.slices > 1) {
+    if (sp.nsplit) {
+        p.sk_first = sp.first;
+        p.sk_tiles = sp.tiles;
+        p.sk_slices = 2;
+        p.sk_nsplit = 1;
+        p.total_units = sp.first + 2 * static_cast<int64_t>(sp.tiles);
+    } else if (sp.slices > 1) {
         // partial sums of every slice, then one arrival counter per (split tile, CTA, epilogue warp)
         const size_t partial = static_cast<size_t>(sp.tiles) * sp.slices * v.tile_m * v.bn * sizeof(float);
         n_counters = sp.tiles * v.cta_group * tg::NUM_EPI_WARPS;

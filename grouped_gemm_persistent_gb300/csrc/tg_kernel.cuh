@@ -132,6 +132,9 @@ struct Params {
     int64_t sk_first;
     int32_t sk_tiles;
     int32_t sk_slices;          // 0: no split
+    // 1: the split tiles are cut into two column halves instead (BN/2-wide MMAs take
+    // half the time; no partial sums): units sk_first + h * sk_tiles + j, h = 0, 1.
+    int32_t sk_nsplit;
     float* sk_partial;          // [sk_tiles][sk_slices][CTA_GROUP][4 warps][BN/4][32 lanes][4]
     uint32_t* sk_count;         // [sk_tiles][CTA_GROUP][4 warps]
 };
@@ -199,6 +202,9 @@ struct TileCoord {
     // columns [0, BN/2) in TMEM lanes 0-63 and [BN/2, BN) in lanes 64-127, both in
     // TMEM columns [0, BN/2).
     bool half;
+    // N-split unit (dense): columns [n0, n0 + BN/2) only, by MMAs of N = BN/2; the
+    // accumulator holds them in TMEM columns [0, BN/2) with the usual row layout.
+    bool nhalf;
 };
 
 // Device-counts MoE schedule, built in shared memory by every CTA at start:
@@ -254,6 +260,7 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     TileCoord c;
     c.g = g;
     c.half = false;
+    c.nhalf = false;
     if constexpr (Cfg::CTA_GROUP == 2 && (Cfg::GROUPED || Cfg::MOE)) {
         const int rows_left = (Cfg::MOE ? mt.row_off[g + 1] - mt.row_off[g] : pr.M) - mb * Cfg::TILE_M;
         c.half = rows_left <= BM;
@@ -275,14 +282,19 @@ struct Work {
     int kb0;      // split tiles: k-blocks [kb0, kb1); whole tiles use the problem's k_blocks
     int kb1;
     int slice;
-    int tail;     // index among the split tiles, or -1 for a whole tile
+    int tail;     // index among the K-split tiles, or -1 for a whole tile
+    int nh;       // column half (0 or 1) of an N-split tile, or -1 for the whole width
 };
 
 template <class Cfg>
 __device__ __forceinline__ Work work_of(const Params& p, int64_t u) {
-    Work w{u, 0, 0, 0, -1};
+    Work w{u, 0, 0, 0, -1, -1};
     if constexpr (!Cfg::GROUPED && !Cfg::MOE) {
-        if (p.sk_slices > 1 && u >= p.sk_first) {
+        if (p.sk_nsplit && u >= p.sk_first) {
+            const int64_t v = u - p.sk_first;
+            w.t = p.sk_first + v % p.sk_tiles;
+            w.nh = static_cast<int>(v / p.sk_tiles);
+        } else if (p.sk_slices > 1 && u >= p.sk_first) {
             const int64_t v = u - p.sk_first;
             const int S = p.sk_slices;
             const int kbs = p.dense.k_blocks;
@@ -294,6 +306,16 @@ __device__ __forceinline__ Work work_of(const Params& p, int64_t u) {
         }
     }
     return w;
+}
+
+// Coordinates of a work unit: its tile's, narrowed to one column half for N-split units.
+template <class Cfg>
+__device__ __forceinline__ TileCoord coord_of(const Params& p, const Work& w, int g, uint32_t rank,
+                                              const MoeTable& mt = {}) {
+    TileCoord c = tile_coord<Cfg>(p, w.t, g, rank, mt);
+    c.nhalf = w.nh >= 0;
+    if (c.nhalf) c.n0 += w.nh * (Cfg::BN / 2);
+    return c;
 }
 
 // ----------------------------------------------------------------------------------------
@@ -528,8 +550,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         g_fenced = g;
                     }
                 }
-                const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
-                const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // first B column this CTA loads
+                const TileCoord tc = coord_of<Cfg>(p, w, g, rank, mt);
+                // first B column this CTA loads (an N-split unit uses the first half of each CTA's box)
+                const int nb0 = tc.n0 + static_cast<int>(rank) * (tc.nhalf ? Cfg::BN_CTA / 2 : Cfg::BN_CTA);
                 const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
                 for (int kb = w.kb0; kb < kb_end; ++kb) {
                     if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, u, stage)) {
@@ -619,9 +642,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const Work w = work_of<Cfg>(p, u);
                 g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
-                // half tiles: M = 128 for the pair (bits 24-28 of the instruction descriptor hold M >> 4)
-                const bool half = tile_coord<Cfg>(p, w.t, g, rank, mt).half;
-                const uint32_t idesc = half ? (pr.idesc & ~(0x1Fu << 24)) | ((128u >> 4) << 24) : pr.idesc;
+                // half tiles: M = 128 for the pair (bits 24-28 of the instruction descriptor hold M >> 4);
+                // N-split units: N = BN/2 (bits 17-22 hold N >> 3)
+                const TileCoord tcm = coord_of<Cfg>(p, w, g, rank, mt);
+                uint32_t idesc = pr.idesc;
+                if (tcm.half) idesc = (idesc & ~(0x1Fu << 24)) | ((128u >> 4) << 24);
+                if (tcm.nhalf) idesc = (idesc & ~(0x3Fu << 17)) | ((static_cast<uint32_t>(BN / 2) >> 3) << 17);
                 if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, u, 16 + acc)) {
                     aborted = true;
                     break;
@@ -702,7 +728,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     g_fenced = g;
                 }
             }
-            const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
+            const TileCoord tc = coord_of<Cfg>(p, w, g, rank, mt);
             // half tiles: warps q and q + 2 share rows (q % 2) * 32 .. + 32 of this CTA's 64,
             // warp q / 2 == 1 taking columns [BN/2, BN)
             const int row0 = tc.m0 + (tc.half ? (q % 2) * 32 : q * 32);
@@ -751,7 +777,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             constexpr int CHUNKS = BN / Cfg::CW;
-            const int n_chunks = tc.half ? CHUNKS / 2 : CHUNKS;
+            const int n_chunks = (tc.half || tc.nhalf) ? CHUNKS / 2 : CHUNKS;
 
             // accumulator columns [c * CW, (c + 1) * CW) of this lane's row; the last chunk
             // hands the TMEM buffer back to the MMA issuer

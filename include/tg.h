@@ -34,12 +34,14 @@
  *  - Degenerate sizes: M == 0 or N == 0 is a no-op returning TG_OK.  K == 0
  *    is the empty sum: C = epilogue(0), i.e. zeros, bias, or GELU(bias).
  *  - Results are deterministic: two identical calls write bitwise-identical C.
- *    Dense calls may compute the tiles of their last, partial wave as several
- *    K-ranges on different SMs; those fp32 partials are added in a fixed
- *    order (an atomic counter only picks which SM does the adding), so the
- *    result does not depend on timing.  Set TG_SPLIT_TAIL=0 in the
- *    environment to turn this off (one K-order per tile, as grouped calls).
- *  - Dense calls with split tiles take a workspace from a library-owned
+ *    Dense calls split the tiles of their last, partial wave: into two column
+ *    halves when there is room (256-wide tiles; the arithmetic per element is
+ *    unchanged), else into several K-ranges on different SMs whose fp32
+ *    partials are added in a fixed order (an atomic counter only picks which
+ *    SM does the adding), so the result does not depend on timing.  Set
+ *    TG_SPLIT_TAIL=0 in the environment to turn splitting off (one K-order per
+ *    tile, as grouped calls), TG_SPLIT_TAIL=k to always cut along K.
+ *  - Dense calls with K-range splits take a workspace from a library-owned
  *    stream-ordered memory pool (at most (resident CTAs) x 128 KiB, released
  *    on the stream after the launch).
  */

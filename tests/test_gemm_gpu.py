@@ -533,12 +533,14 @@ def test_timeline_trace_records_every_tile(tile):
 
 
 # ------------------------------------------------------------------------------------------ split tiles
-# The last, partial wave of a dense launch is cut along K: each of its tiles is
-# computed by several CTAs (pairs) at once and the last to finish adds the fp32
-# partials in slice order.  Shapes below: (a) more tiles than resident pairs, with
-# a small remainder (2304^2: 81 pair tiles on 76 pairs, 5 tiles split 4 ways);
-# (b) fewer tiles than CTAs (512^2 x 2048: 8 tiles split 8 ways); (c) a ragged
-# tail in M, N and K.
+# The last, partial wave of a dense launch is split.  With 256-wide tiles and
+# room for twice its tiles, each tile becomes two column halves (N = 128 MMAs).
+# Otherwise each tile is cut along K and computed by several CTAs (pairs) at
+# once; the last to finish adds the fp32 partials in slice order
+# (TG_SPLIT_TAIL=k forces the K-cut).  Shapes below: (a) more tiles than
+# resident pairs, with a small remainder (2304^2: 81 pair tiles on 76 pairs);
+# (b) fewer tiles than CTAs (512^2 x 2048: 8 tiles split 8 ways along K); (c) a
+# ragged tail in M, N and K.
 
 SPLIT_SHAPES = [(2304, 2304, 1024), (512, 512, 2048), (1000, 776, 1480)]
 
@@ -576,14 +578,32 @@ def test_split_tail_integer_exact_bitwise():
 
 
 @pytest.mark.parametrize("tile_shape", TILES)
-def test_split_tail_every_variant(tile_shape, monkeypatch):
+@pytest.mark.parametrize("mode", ["auto", "k"])
+def test_split_tail_every_variant(tile_shape, mode, monkeypatch):
+    # 640x520x1536: fewer tiles than CTAs; 2304^2 x 1024: one or two full waves and a
+    # remainder (column halves for 256-wide tiles, K-ranges for 128-wide or forced)
     monkeypatch.setenv("TG_TILE", tile_shape)
-    for a_col, b_col in LAYOUTS:
-        case = wl.dense_random(640, 520, 1536, seed=44, dist="uniform", a_col_major=a_col, b_col_major=b_col,
-                               epi="bias", **lds(640, 520, 1536, a_col, b_col))
-        c = run_dense(case)
-        _sync_ok()
-        check_dense(case, c)
+    if mode == "k":
+        monkeypatch.setenv("TG_SPLIT_TAIL", "k")
+    for M, N, K in [(640, 520, 1536), (2304, 2304, 1024)]:
+        for a_col, b_col in LAYOUTS:
+            case = wl.dense_random(M, N, K, seed=44, dist="uniform", a_col_major=a_col, b_col_major=b_col,
+                                   epi="bias", **lds(M, N, K, a_col, b_col))
+            c = run_dense(case)
+            _sync_ok()
+            check_dense(case, c)
+
+
+def test_split_tail_k_ranges_after_full_waves(monkeypatch):
+    # K-cut of the remainder after a full wave: deterministic, integer-exact
+    monkeypatch.setenv("TG_SPLIT_TAIL", "k")
+    case = wl.dense_random(2304, 2304, 1024, seed=45, dist="int4", c_dtype="f32")
+    y, _ = oracle_dense(case)
+    c1 = run_dense(case)
+    c2 = run_dense(case)
+    _sync_ok()
+    assert torch.equal(c1, c2)
+    assert np.array_equal(to_f64(c1), y)
 
 
 # ------------------------------------------------------------------------------------------ full-size workloads
