@@ -570,7 +570,10 @@ SplitPlan plan_split(int64_t tiles, int units, int k_blocks, int bn) {
     if (units <= 0) return sp;
     const int64_t R = tiles % units;
     if (R == 0) return sp;
-    if (bn == 256 && tiles > units && 2 * R <= units && !(env && env[0] == 'k')) {
+    // Column halves still load the whole A box for half the MMA time; measured on GB300
+    // they beat K-ranges at 64 k-blocks (4096^3) and lose at 128 (8192^3), where the
+    // K-ranges' add-up costs relatively less.
+    if (bn == 256 && tiles > units && 2 * R <= units && k_blocks <= 96 && !(env && env[0] == 'k')) {
         sp.first = tiles - R;
         sp.tiles = static_cast<int>(R);
         sp.slices = 2;

@@ -554,6 +554,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 // first B column this CTA loads (an N-split unit uses the first half of each CTA's box)
                 const int nb0 = tc.n0 + static_cast<int>(rank) * (tc.nhalf ? Cfg::BN_CTA / 2 : Cfg::BN_CTA);
                 const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
+                // N-split units with N-contiguous B load only the 64-column boxes they use
+                const int b_boxes = (Cfg::B_MN && tc.nhalf) ? Cfg::BN_CTA / 128 : Cfg::BN_CTA / 64;
+                const uint32_t stage_tx = (Cfg::A_BYTES + (Cfg::B_MN ? b_boxes * 8192 : Cfg::B_BYTES)) * CG;
                 for (int kb = w.kb0; kb < kb_end; ++kb) {
                     if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, u, stage)) {
                         aborted = true;
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     const bool skip = withhold && kb == p.withhold_kb;
                     if (!skip) {
                         const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
-                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::STAGE_BYTES * CG);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         const int k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * Cfg::A_BYTES;
                         const uint32_t b_dst = sB + stage * Cfg::B_BYTES;
@@ -583,13 +586,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             };
                             if constexpr (Cfg::B_MN) {
 #pragma unroll
-                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load3(b_dst + j * 8192, nb0 + j * 64, k0);
+                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
+                                    if (j < b_boxes) load3(b_dst + j * 8192, nb0 + j * 64, k0);
                             } else {
                                 load3(b_dst, k0, nb0);
                             }
                         } else if constexpr (Cfg::B_MN) {
 #pragma unroll
-                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
+                                if (j < b_boxes) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
                         } else {
                             load(b_dst, &pr.tma_b, k0, nb0);
                         }
