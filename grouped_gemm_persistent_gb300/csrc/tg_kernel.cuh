@@ -8,10 +8,11 @@
 //
 //   warp 0      TMA producer: one thread streams A and B k-blocks into a
 //               STAGES-deep ring; full[s] completes when the bytes land.
-//   warp 1      MMA issuer: one thread waits full[s], issues BK/16 tcgen05.mma
-//               into TMEM accumulator buffer b, commits empty[s] (slot free)
-//               and, after the last k-block, tfull[b] (tile done).  Warp 1
-//               also allocates and frees tensor memory.
+//   warp 1      MMA issuer: the converged warp waits full[s]; lane 0 alone (a
+//               guard predicate, no branch) issues BK/16 tcgen05.mma into TMEM
+//               accumulator buffer b and commits empty[s] (slot free) and,
+//               after the last k-block, tfull[b] (tile done).  Warp 1 also
+//               allocates and frees tensor memory.
 //   warps 2-5   epilogue: wait tfull[b], tcgen05.ld the fp32 accumulator,
 //               release the buffer (tempty[b]), add bias / apply GELU(tanh),
 //               round, stage through swizzled shared memory and TMA-store C.
@@ -22,10 +23,13 @@
 // tcgen05.mma.cta_group::2 over both, and each CTA's TMEM receives its 128
 // rows of the accumulator.  No TMA multicast is used.
 //
-// The tile scheduler is static and persistent: work unit u (a CTA, or a CTA
-// pair) takes tiles u, u + U, u + 2U, ... of the concatenated tile list of
-// all problems; within a problem tiles are rastered in bands of `band`
-// N-tiles so that concurrently running tiles share A rows and B columns in L2.
+// The tile scheduler is static and persistent: CTA (pair) i takes work units
+// i, i + U, i + 2U, ... of the concatenated tile list of all problems; within a
+// problem tiles are rastered in bands of `band` N-tiles so that concurrently
+// running tiles share A rows and B columns in L2.  A work unit is a tile,
+// except in a dense launch's last, partial wave, whose tiles are split into
+// column halves or K-ranges (Params::sk_*).  In grouped and MoE launches a
+// problem's last M-tile with at most 128 rows is a half tile (M = 128 MMAs).
 //
 // Every mbarrier wait is bounded (wait_budget_ns, measured with %globaltimer).
 // On expiry the waiting thread records the failure in the device error
@@ -50,7 +54,7 @@ constexpr int UMMA_K = 16;           // K per tcgen05.mma.kind::f16
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;         // warps 2..5 drain TMEM; warp w reads lanes 32*(w%4)..+31
 constexpr int NUM_EPI_WARPS = 4;
-constexpr int FIX_BUFS = 4;    // chunks in flight per warp while adding up a split tile
+constexpr int FIX_BUFS = 4;          // chunks in flight per warp while adding up a split tile
 constexpr int C_STAGE_BYTES = 32 * 128;   // per-warp store staging buffer: 32 rows x 128 bytes
 constexpr int SMEM_LIMIT = 232448;        // max dynamic shared memory per CTA on sm_100 family
 constexpr int MOE_MAX_G = 190;            // experts per call of the device-counts MoE form (table in shared memory)
