@@ -10,7 +10,8 @@ each one launch of the persistent kernel through the C ABI.  value = FLOPs of
 the step / device time of the step (CUDA events on the launching stream).
 L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer outside
 the timed events.  `e2e` times the same steps through the public API with the
-inputs copied from pinned host memory every step and C read back.
+inputs copied from pinned host memory every step and C read back, pipelined
+across two device buffer sets (step i's upload overlaps step i-1's kernels).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
