@@ -1,9 +1,9 @@
 /*
  * tg.h - C ABI of libtg: bf16 GEMM and grouped GEMM on NVIDIA GB300 (sm_103a).
  *
- * What is computed.  C = epilogue(A . B) with bf16 operands, an fp32
- * accumulator summed over K in BLOCK_K steps, and an epilogue fused into the
- * same kernel: none, + bias, or + bias then GELU(tanh).  This is the tiled
+ * What is computed.  C = epilogue(A . B) with bf16 (or fp16) operands, an
+ * fp32 accumulator summed over K in BLOCK_K steps, and an epilogue fused into
+ * the same kernel: none, + bias, or + bias then GELU(tanh).  This is the tiled
  * matmul that "How We Built TLX: A Hardware-Native GPU Compiler for Production
  * ML at Scale" uses as its running example (section "Introducing TLX": the
  * standard Triton listing fixes the arithmetic, the TLX-on-Blackwell listing
@@ -11,6 +11,9 @@
  * TileGym/cuTile tutorial page.  The grouped form is the MoE expert GEMM of
  * the same TLX article's third case study ("Distributed grouped GEMM for LLM
  * pre-training"): one problem per expert, ragged M, one persistent launch.
+ * Around these sit a broadcast form for repeated A rows, an MoE form whose
+ * token counts stay in device memory, and an RMS-normalised form (the
+ * normalisation applied as a per-row factor in the epilogue).
  *
  * Where it runs.  One persistent, warp-specialised CUDA kernel on the
  * current device: a TMA producer warp fills a shared-memory ring guarded by
