@@ -8,7 +8,8 @@ One step = one pass of the whole hot path over one batch of synthetic input:
     Dirichlet(0.5) multinomial (seed 3), bf16 out,
 each one launch of the persistent kernel through the C ABI.  value = FLOPs of
 the step / device time of the step (CUDA events on the launching stream).
-L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer outside
+L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer (and then
+reading another, so the written lines go back to HBM before the next step) outside
 the timed events.  `e2e` times the same steps through the public API with the
 inputs copied from pinned host memory every step and C read back, pipelined
 across two device buffer sets (step i's upload overlaps step i-1's kernels).
@@ -376,6 +377,9 @@ def run_ours(args, parts_names):
     log(f"[bench] inputs ready in {time.perf_counter() - t0:.1f} s")
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    # read after the flush write: evicts the write's dirty lines, so their write-back to
+    # HBM happens here and not inside the next timed step
+    flush_read = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     step_flops = sum(p.flops for p in parts)
 
     for _ in range(args.warmup):
@@ -391,6 +395,7 @@ def run_ours(args, parts_names):
         for i in range(args.steps):
             if not args.warm:
                 flush.zero_()                 # L2 flush, outside the timed events
+                flush_read.sum()
             ev[i][0].record(stream)
             for j, p in enumerate(parts):
                 launches += p.launch(stream)
@@ -507,7 +512,9 @@ def run_ours(args, parts_names):
         "metric": METRIC, "value": agg["value_tflops"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": agg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": args.workload, "parts": parts_out, "l2": "warm (not flushed between steps)" if args.warm else "flushed between steps (256 MiB write)",
+        "config": {"workload": args.workload, "parts": parts_out, "l2": "warm (not flushed between steps)" if args.warm else
+                   "flushed between steps (256 MiB write, then a 256 MiB read that evicts its dirty lines), "
+                   "outside the timed events",
                    "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
                    "frac_of_peak": agg["value_tflops"] / (world * peak)},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
