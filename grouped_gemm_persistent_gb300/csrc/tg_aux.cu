@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(RMS_WARPS * 32) row_rms_kernel(const uint16_t*
                                                                   int n_counters) {
     // the fused GEMM launched after this kernel may start its set-up and main loop now;
     // it waits for this grid's completion only before reading r (and the counters)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    ptx::grid_launch_dependents();
     clear_counters(counters, n_counters);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(RMS_WARPS * 32) row_rms_kernel(const uint16_t*
 }
 
 __global__ void __launch_bounds__(256) clear_counters_kernel(uint32_t* counters, int n) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    ptx::grid_launch_dependents();
     clear_counters(counters, n);
 }
 

@@ -109,11 +109,6 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Named barrier for a subset of warps of this CTA.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
-    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
-}
-
 // ----------------------------------------------------------------------------------------
 // TMA
 
@@ -212,35 +207,19 @@ __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T with an fp32 accumulator, shapes from the instruction
-// descriptor.  No "memory" clobber: the MMA touches no memory the compiler tracks, and
-// volatile asm keeps its order relative to the barrier waits and commits around it.
-template <int CTA_GROUP>
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    if constexpr (CTA_GROUP == 1)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.u32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-    else
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.u32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-            :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-}
-
 // Arrive once on `bar` (this CTA) when all MMAs issued so far by this thread are complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(bar));
 }
 
-// The same two, executed by every lane of a converged warp with only the lanes that have
-// `issue` set performing them (a guard predicate instead of a branch): the issuing warp
-// never diverges, and the per-k-block cost of reconverging is gone.
+// D[tmem] (+)= A[smem] . B[smem]^T with an fp32 accumulator, shapes from the instruction
+// descriptor, and its commit (arrive on an mbarrier when all MMAs issued so far by the
+// thread are complete).  Executed by every lane of a converged warp, performed only by
+// the lanes with `issue` set (a guard predicate instead of a branch): the issuing warp
+// never diverges, and the per-k-block cost of reconverging is gone.  No "memory"
+// clobber: the MMA touches no memory the compiler tracks, and volatile asm keeps its
+// order relative to the barrier waits and commits around it.
 template <int CTA_GROUP>
 __device__ __forceinline__ void mma_bf16_guarded(bool issue, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate) {
