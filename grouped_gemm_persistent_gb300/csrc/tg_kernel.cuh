@@ -403,11 +403,14 @@ __device__ __forceinline__ void sleep_ns(uint64_t ns) {
 // epilogue math
 
 __device__ __forceinline__ float gelu_tanh_f32(float z) {
-    // z/2 * (1 + tanh(sqrt(2/pi) * (z + 0.044715 z^3)))
-    const float k0 = 0.7978845608028654f;
-    const float k1 = 0.044715f;
-    const float u = k0 * fmaf(k1 * z, z * z, z);
-    return 0.5f * z * (1.0f + ptx::tanh_approx(u));
+    // z/2 * (1 + tanh(sqrt(2/pi) * (z + 0.044715 z^3))), arranged for few instructions
+    // (the epilogue warps share issue slots with the MMA issuer):
+    //   u = z * (k0 + k0 k1 z^2),  gelu = h + h * tanh(u) with h = z / 2
+    const float k0 = 0.7978845608028654f;               // sqrt(2 / pi)
+    const float k01 = 0.7978845608028654f * 0.044715f;  // sqrt(2 / pi) * 0.044715
+    const float u = z * fmaf(k01, z * z, k0);
+    const float h = 0.5f * z;
+    return fmaf(h, ptx::tanh_approx(u), h);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
