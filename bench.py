@@ -325,12 +325,19 @@ def oracle_sample(parts, target_s: float, seed: int = 0):
 # ------------------------------------------------------------------------------------------
 # arms
 
+def reference_step_seconds(steps: int, warmup: int) -> float:
+    """Oracle work per timed step of the reference arm: about 150 s for the whole run
+    (warm-up steps count a quarter), whatever --steps and --warmup are, between 0.01 s
+    (at least one small row sample of every part) and 10 s per step."""
+    return max(0.01, min(10.0, 150.0 / max(1.0, steps + warmup / 4)))
+
+
 def run_reference(args, parts_names):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     parts = [Part(n) for n in parts_names]
-    per_step_s = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step_s = reference_step_seconds(args.steps, args.warmup)
     for _ in range(args.warmup):
         oracle_sample(parts, per_step_s / 4)
     times, flops = [], 0
@@ -340,7 +347,7 @@ def run_reference(args, parts_names):
         flops += r["flops"]
     total = sum(times)
     value = flops / total / 1e12
-    sample = (f"each step: oracle (fp64 CPU) on random output rows of every part, about {per_step_s:.1f} s of work; "
+    sample = (f"each step: oracle (fp64 CPU) on random output rows of every part, about {per_step_s:.3f} s of work; "
               f"last step rows {r['rows']}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,

@@ -77,3 +77,12 @@ def test_reference_arm_other_ranks_exit_quietly():
                           "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
     assert out.returncode == 0
     assert out.stdout.strip() == ""
+
+
+def test_reference_arm_stays_within_minutes():
+    import bench
+    for steps, warmup in [(3000, 50), (1, 0), (20, 3), (100000, 10)]:
+        per = bench.reference_step_seconds(steps, warmup)
+        total = per * (steps + warmup / 4)
+        assert 0.01 <= per <= 10.0
+        assert total <= 160.0 or per == 0.01, (steps, warmup, total)
