@@ -85,4 +85,4 @@ def test_reference_arm_stays_within_minutes():
         per = bench.reference_step_seconds(steps, warmup)
         total = per * (steps + warmup / 4)
         assert 0.01 <= per <= 10.0
-        assert total <= 110.0 or per == 0.01, (steps, warmup, total)
+        assert total <= 70.0 or per == 0.01, (steps, warmup, total)
