@@ -3,9 +3,11 @@
 // Responsibilities: argument checks (before anything is enqueued), TMA tensor
 // map encoding (cuTensorMapEncodeTiled, reached through the runtime's driver
 // entry-point query so the library does not link libcuda), choice of kernel
-// variant and persistent grid size, the grouped problem table (prefix sums of
-// tile counts, copied into a stream-ordered workspace), and the per-device
-// error record written by the kernels' bounded waits.
+// variant and persistent grid size, the split of a dense launch's last wave
+// (column halves or K-ranges, with the K-range workspace and the counter reset
+// before the GEMM), the grouped problem table (prefix sums of tile counts,
+// copied into a stream-ordered workspace), and the per-device error record
+// written by the kernels' bounded waits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
