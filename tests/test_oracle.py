@@ -265,6 +265,12 @@ def test_compare_detects_errors():
     assert oracle.compare(y, y, s)["ok"]
     assert not oracle.compare(y + 0.05, y, s)["ok"]
     assert not oracle.compare(np.array([[np.nan, 2.0]]), y, s)["ok"]
+    # an all-NaN result is reported as bad (worst element found), not an exception
+    import warnings
+    with warnings.catch_warnings():
+        warnings.simplefilter("ignore", RuntimeWarning)
+        r = oracle.compare(np.full((1, 2), np.nan), y, s)
+    assert not r["ok"] and r["n_bad"] == 2 and r["worst"] is not None
 
 
 # ----------------------------------------------------------------------------------------
