@@ -200,3 +200,25 @@ def test_rmsnorm_argument_checks(lib):
     assert fused(A=None) == tg.TG_ERR_INVALID_ARG
     assert fused(ldb=32) == tg.TG_ERR_INVALID_ARG
     assert fused(epi=1) == tg.TG_ERR_INVALID_ARG                        # bias epilogue without a bias
+
+
+def _declared_arity():
+    """Parameter count of every function prototype in include/tg.h."""
+    import re
+    text = open(_binding.HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    arity = {}
+    for name, params in re.findall(r"\b(tg_[a-z_]+)\s*\(([^)]*)\)\s*;", text):
+        params = params.strip()
+        arity[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return arity
+
+
+def test_binding_argtypes_match_header_arity(lib):
+    # the ctypes prototypes must take as many arguments as the C declarations
+    arity = _declared_arity()
+    assert set(arity) == set(tg.header_functions())
+    for name, n in arity.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name} has no argtypes in the binding"
+        assert len(fn.argtypes) == n, f"{name}: header takes {n} arguments, binding {len(fn.argtypes)}"
