@@ -286,6 +286,9 @@ MUTANTS = {
     "s_not_abs": ("s[j] += fabs(p);", "s[j] += p;"),
     "a_k_reversed": ("A[i * lda + k], in_dtype);", "A[i * lda + (K - 1 - k)], in_dtype);"),
     "norm_sum_not_mean": ("scale = 1.0 / sqrt(ss / (double)K + eps);", "scale = 1.0 / sqrt(ss + eps);"),
+    "norm_abs_not_square": ("ss += a * a;", "ss += fabs(a);"),
+    "gelu_half_dropped": ("return 0.5 * z * (1.0 + tanh(", "return z * (1.0 + tanh("),
+    "gelu_tanh_sign": ("(1.0 + tanh(c * (z + 0.044715 * z * z * z)))", "(1.0 - tanh(c * (z + 0.044715 * z * z * z)))"),
     "norm_eps_dropped": ("scale = 1.0 / sqrt(ss / (double)K + eps);", "scale = 1.0 / sqrt(ss / (double)K);"),
     "f16_exponent_bias": ("v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);"),
     "f16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
