@@ -120,7 +120,8 @@ tg_status tg_gemm(const void *A, tg_layout layout_a, int64_t lda,
  * broadcasts inside the kernel.  Each distinct result row is computed once per
  * replica CTA and stored `repeat` times, so A costs U*K*2 bytes of traffic
  * instead of U*repeat*K*2.  Results are bitwise identical to tg_gemm on the
- * materialised A.
+ * materialised A when that call does not split its last wave along K (always
+ * with TG_SPLIT_TAIL=0), and within the stated tolerance otherwise.
  *
  *   A_user, layout_a, lda : bf16 U x K (row-major: lda >= K; column-major: lda >= U).
  *   repeat                : >= 1; U * repeat < 2^31.
