@@ -3,11 +3,14 @@
 
 One step = one pass of the whole hot path over one batch of synthetic input:
   * dense GEMM M=N=K=4096, A row-major, B column-major, U(-1,1), fused
-    bias + GELU(tanh), bf16 out (seed 1), and
+    bias + GELU(tanh), bf16 out (seed 1),
+  * dense GEMM M=N=K=8192, A and B row-major, N(0,1)/sqrt(K), fp32 out (seed 2), and
   * grouped MoE GEMM, 64 experts, K=4096, N=1536, 65536 tokens split by a
     Dirichlet(0.5) multinomial (seed 3), bf16 out,
-each one launch of the persistent kernel through the C ABI.  value = FLOPs of
-the step / device time of the step (CUDA events on the launching stream).
+each one launch of the persistent kernel through the C ABI (plus the small
+counter reset before a dense stream-K launch).  Each part is timed with CUDA
+events on the launching stream every step; value = FLOPs of the step / the sum
+of the parts' median step times (mean, p10 and p90 are reported beside it).
 L2 (129 MB) is flushed between timed steps by writing a 256 MiB buffer (and then
 reading another, so the written lines go back to HBM before the next step) outside
 the timed events.  `e2e` times the same steps through the public API with the
@@ -37,9 +40,10 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-HEADLINE = "dense4096_bias_gelu+grouped_moe"
+HEADLINE = "dense4096_bias_gelu+dense8192_f32+grouped_moe"
 WORKLOADS = {
-    HEADLINE: ["dense_4096_bias_gelu", "grouped_moe"],
+    HEADLINE: ["dense_4096_bias_gelu", "dense_8192_f32", "grouped_moe"],
+    "dense4096_bias_gelu+grouped_moe": ["dense_4096_bias_gelu", "grouped_moe"],
     "dense_4096_bias_gelu": ["dense_4096_bias_gelu"],
     "dense_8192_f32": ["dense_8192_f32"],
     "grouped_moe": ["grouped_moe"],
@@ -157,21 +161,32 @@ class ClockSampler:
         pmax = max(r[2] for r in rows)
         loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
         return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "power_w_max": pmax}
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded), "power_w_max": pmax}
 
 
 def recorded_traffic(kernel_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel source."""
-    from grouped_gemm_persistent_gb300.build import _digest
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel code
+    (the digest ignores comments, so documentation edits keep the record valid)."""
+    from grouped_gemm_persistent_gb300.build import code_digest
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = _digest([])[:16]
+    digest = code_digest()[:16]
     for line in open(path):
         parts = line.split()
         if len(parts) == 4 and parts[0] == "traffic" and parts[1] == kernel_key and parts[2] == digest:
             return int(parts[3])
     return None
+
+
+# ------------------------------------------------------------------------------------------
+# statistics of per-step times
+
+def step_stats(ms: list[float]) -> dict:
+    """Median, mean and the 10th / 90th percentiles of per-step times (ms)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "mean": float(a.mean()), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "min": float(a.min()), "max": float(a.max()), "n": int(a.size)}
 
 
 # ------------------------------------------------------------------------------------------
@@ -272,12 +287,10 @@ class Part:
             b = d["b"].t() if c.b_col_major else d["b"]
             tg.gemm_rmsnorm(d["a"], b, RMS_EPS, d["out"], row_scale=d["row_scale"], bias=d.get("bias"),
                             epilogue=c.epi, stream=stream)
-            return 2   # row statistics + GEMM
         else:
             a = d["a"].t() if c.a_col_major else d["a"]
             b = d["b"].t() if c.b_col_major else d["b"]
             tg.gemm(a, b, d["out"], bias=d.get("bias"), epilogue=c.epi, stream=stream)
-        return 1   # kernel launches made (one class of layouts per grouped call)
 
 
     # -- oracle side (CPU baseline): rows of this part, FLOPs done
@@ -419,7 +432,7 @@ def run_ours(args, parts_names):
     tg.device_status(stream)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(args.steps)]
-    launches = 0
+    launches0 = tg.launch_count()
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize()
@@ -429,13 +442,15 @@ def run_ours(args, parts_names):
                 flush_read.sum()
             ev[i][0].record(stream)
             for j, p in enumerate(parts):
-                launches += p.launch(stream)
+                p.launch(stream)
                 ev[i][j + 1].record(stream)
         torch.cuda.synchronize()
         barrier(world)
+    launches = tg.launch_count() - launches0      # kernels of this library enqueued in the timed region
     tg.device_status(stream)
     part_ms = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(len(parts))]
-    step_ms = sum(statistics.fmean(x) for x in part_ms)
+    part_stats = [step_stats(x) for x in part_ms]
+    step_ms = sum(st["median"] for st in part_stats)
     agg = aggregate(gather_max(step_ms, world), step_flops)
 
     # End to end through the public API: every step copies its inputs from pinned host
@@ -453,7 +468,7 @@ def run_ours(args, parts_names):
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
 
         def e2e_loop(n_steps):
-            launches_n = 0
+            launches_n = tg.launch_count()
             for i in range(n_steps):
                 k = i % 2
                 with torch.cuda.stream(s_in):
@@ -466,14 +481,14 @@ def run_ours(args, parts_names):
                 if i >= 2:
                     stream.wait_event(d2h_done[k])           # step i - 2's C has left set k
                 for p in parts:
-                    launches_n += p.launch(stream, k)
+                    p.launch(stream, k)
                 comp_done[k].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(comp_done[k])
                     for p in parts:
                         p.d2h(k)
                     d2h_done[k].record(s_out)
-            return launches_n
+            return tg.launch_count() - launches_n
 
         e2e_loop(2)                                          # warm-up
         torch.cuda.synchronize()
@@ -507,9 +522,9 @@ def run_ours(args, parts_names):
     timed_s = sum(sum(x) for x in part_ms) * 1e-3
     sustained = timed_s >= 1.0 and "bf16_tflops_sustained" in peaks
     # dominant kernel: the part with the largest device time
-    dom = max(range(len(parts)), key=lambda j: statistics.fmean(part_ms[j]))
+    dom = max(range(len(parts)), key=lambda j: part_stats[j]["median"])
     dp = parts[dom]
-    dom_ms = statistics.fmean(part_ms[dom])
+    dom_ms = part_stats[dom]["median"]
     peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     peak_kind = "bf16_tflops_sustained (timed region %.1f s)" % timed_s if sustained else "bf16_tflops (burst)"
     traffic = recorded_traffic(dp.name)
@@ -535,10 +550,12 @@ def run_ours(args, parts_names):
 
     parts_out = []
     for j, p in enumerate(parts):
-        ms = statistics.fmean(part_ms[j])
-        parts_out.append({**p.describe(), "ms": ms, "tflops": p.flops / (ms * 1e-3) / 1e12,
+        st = part_stats[j]
+        ms = st["median"]
+        tf = p.flops / (ms * 1e-3) / 1e12
+        parts_out.append({**p.describe(), "ms": ms, "ms_stats": st, "tflops": tf,
                           "gbs": p.bytes / (ms * 1e-3) / 1e9, "algorithmic_bytes": p.bytes,
-                          "frac_of_peak": p.flops / (ms * 1e-3) / 1e12 / peak,
+                          "frac_of_peak": tf / peak, "frac_of_burst_peak": tf / peaks["bf16_tflops"],
                           "roofline_ms": 1e3 * max(p.flops / (peak * 1e12), p.bytes / (peaks["hbm_gbs"] * 1e9))})
     clk = clocks.summary()
     line = {
@@ -551,7 +568,8 @@ def run_ours(args, parts_names):
                    "parallelism": f"independent replicas x{world}" if world > 1 else "single GPU",
                    "frac_of_peak": agg["value_tflops"] / (world * peak)},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
+                   "samples": clk["samples"], "samples_under_load": clk.get("samples_under_load")},
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -95,10 +95,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.tg_set_wait_budget_ms.argtypes = [ctypes.c_uint32]
         lib.tg_debug_withhold_stage.restype = ci
         lib.tg_debug_withhold_stage.argtypes = [i64]
+        lib.tg_debug_withhold_stage_in.restype = ci
+        lib.tg_debug_withhold_stage_in.argtypes = [i64, ctypes.c_int32]
         lib.tg_debug_trace.restype = ci
         lib.tg_debug_trace.argtypes = [vp, i64, vp, i64]
         lib.tg_version.restype = ctypes.c_uint32
         lib.tg_version.argtypes = []
+        lib.tg_launch_count.restype = ctypes.c_uint64
+        lib.tg_launch_count.argtypes = []
         if path is None:
             _lib = lib
         return lib
@@ -370,19 +374,25 @@ def set_wait_budget_ms(ms: int) -> None:
     _check(load().tg_set_wait_budget_ms(ms))
 
 
-def debug_withhold_stage(k_block: int) -> None:
-    _check(load().tg_debug_withhold_stage(k_block))
+def debug_withhold_stage(k_block: int, block: int = 0) -> None:
+    """Arm the failure-path test hook for this thread's next launch (tg_debug_withhold_stage_in)."""
+    _check(load().tg_debug_withhold_stage_in(k_block, block))
 
 
 def debug_trace(tile_records: torch.Tensor | None, cta_records: torch.Tensor | None = None) -> None:
     """Arm a timeline trace of this thread's next launch (see tg_debug_trace in include/tg.h).
 
-    ``tile_records`` is an int64 CUDA tensor [T, 4] and ``cta_records`` [B, 2]."""
+    ``tile_records`` is an int64 CUDA tensor [T, 4] and ``cta_records`` [B, 4]."""
     tp = 0 if tile_records is None else tile_records.data_ptr()
     tc = 0 if tile_records is None else tile_records.shape[0]
     cp = 0 if cta_records is None else cta_records.data_ptr()
     cc = 0 if cta_records is None else cta_records.shape[0]
     _check(load().tg_debug_trace(tp or None, tc, cp or None, cc))
+
+
+def launch_count() -> int:
+    """Kernels this thread has enqueued through libtg so far (tg_launch_count)."""
+    return int(load().tg_launch_count())
 
 
 def version() -> tuple[int, int]:

@@ -59,6 +59,46 @@ def _digest(extra_flags) -> str:
     return h.hexdigest()
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and empty lines (string
+    and character literals are kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [l.rstrip() for l in "".join(out).splitlines()]
+    return "\n".join(l for l in lines if l)
+
+
+def code_digest() -> str:
+    """Hash of the kernel and API sources with comments and blank lines taken out: it
+    changes only when the compiled code can change (the key of profiles/traffic.txt)."""
+    h = hashlib.sha256()
+    for d in (CSRC, INCLUDE):
+        for name in sorted(os.listdir(d)):
+            p = os.path.join(d, name)
+            if os.path.isfile(p):
+                h.update(name.encode())
+                with open(p, encoding="utf-8") as f:
+                    h.update(_strip_comments(f.read()).encode())
+    h.update(" ".join(FLAGS).replace(ROOT, "<root>").encode())
+    return h.hexdigest()
+
+
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
     os.makedirs(BUILD, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []

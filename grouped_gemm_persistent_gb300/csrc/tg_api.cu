@@ -3,11 +3,11 @@
 // Responsibilities: argument checks (before anything is enqueued), TMA tensor
 // map encoding (cuTensorMapEncodeTiled, reached through the runtime's driver
 // entry-point query so the library does not link libcuda), choice of kernel
-// variant and persistent grid size, the split of a dense launch's last wave
-// (column halves or K-ranges, with the K-range workspace and the counter reset
-// before the GEMM), the grouped problem table (prefix sums of tile counts,
-// copied into a stream-ordered workspace), and the per-device error record
-// written by the kernels' bounded waits.
+// variant and persistent grid size, the stream-K plan of a dense launch (its
+// partial-sum workspace and the counter reset before the GEMM), the grouped
+// problem table (prefix sums of tile counts, copied into a stream-ordered
+// workspace), and the per-device error record written by the kernels' bounded
+// waits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -30,6 +30,10 @@
 // Per-device record of the first in-kernel wait that ran out (zero at module load).
 __device__ tg::ErrorRecord g_tg_error;
 
+// Problem table of tg_grouped_gemm_noalloc (see that entry point below).
+static __device__ __align__(256) tg::Problem g_noalloc_table[TG_NOALLOC_MAX_PROBLEMS];
+static_assert(sizeof(g_noalloc_table) == 128 * 1024, "the header states a 128 KiB table");
+
 namespace {
 
 using tg::Config;
@@ -41,7 +45,12 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 thread_local std::string t_message;
-thread_local int64_t t_withhold = -1;
+// Test hook armed by tg_debug_withhold_stage(_in): k-block (-1 = off) and block.
+struct WithholdArm {
+    int64_t kb = -1;
+    int32_t block = 0;
+};
+thread_local WithholdArm t_withhold;
 struct TraceArm {
     uint64_t* tiles = nullptr;
     int64_t tiles_cap = 0;
@@ -49,6 +58,7 @@ struct TraceArm {
     int64_t ctas_cap = 0;
 };
 thread_local TraceArm t_trace;
+thread_local uint64_t t_launches = 0;   // kernels this thread has enqueued (tg_launch_count)
 
 std::atomic<uint32_t> g_budget_ms{0};
 
@@ -82,9 +92,11 @@ uint32_t budget_ms() {
 
 struct DeviceState {
     bool ready = false;
+    int dev = 0;
     int cc_major = 0, cc_minor = 0, sms = 0;
     tg::ErrorRecord* err = nullptr;
-    cudaMemPool_t pool = nullptr;
+    cudaMemPool_t pool = nullptr;          // created by the first call that allocates a workspace
+    tg::Problem* noalloc_table = nullptr;  // device address of g_noalloc_table, looked up by the first no-alloc call
     int units[128] = {};  // resident work units per kernel variant (0 = not yet queried)
     int moe_units[16] = {};
 };
@@ -92,6 +104,10 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
+// Checks and addresses of the current device, once per device: compute
+// capability, SM count, and the device address of the error record (in host
+// code a __device__ variable's name is only a stand-in for the symbol).
+// Allocates nothing.
 tg_status device_state(DeviceState** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -100,6 +116,7 @@ tg_status device_state(DeviceState** out) {
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState& d = g_dev[dev];
     if (!d.ready) {
+        d.dev = dev;
         if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
@@ -110,17 +127,32 @@ tg_status device_state(DeviceState** out) {
         void* sym = nullptr;
         if ((e = cudaGetSymbolAddress(&sym, g_tg_error)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
         d.err = static_cast<tg::ErrorRecord*>(sym);
-        cudaMemPoolProps props = {};
-        props.allocType = cudaMemAllocationTypePinned;
-        props.location.type = cudaMemLocationTypeDevice;
-        props.location.id = dev;
-        if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
-        uint64_t keep = UINT64_MAX;  // keep freed workspace cached in the pool
-        if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
-            return cuda_fail(e, "cudaMemPoolSetAttribute");
         d.ready = true;
     }
     *out = &d;
+    return TG_OK;
+}
+
+// The library's stream-ordered memory pool on d's device, created by the first
+// call that needs a workspace (grouped problem tables, stream-K partial sums).
+tg_status device_pool(DeviceState* d, cudaMemPool_t* out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d->pool) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = d->dev;
+        cudaMemPool_t pool = nullptr;
+        cudaError_t e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+        uint64_t keep = UINT64_MAX;  // keep freed workspace cached in the pool
+        if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return cuda_fail(e, "cudaMemPoolSetAttribute");
+        }
+        d->pool = pool;
+    }
+    *out = d->pool;
     return TG_OK;
 }
 
@@ -324,11 +356,26 @@ TileChoice pick_tile(int64_t rows, int64_t max_n, int sms) {
     return t;
 }
 
-// Raster band (N-tiles swept before stepping along M): a square-ish footprint
-// for the tiles that run concurrently, so A rows and B columns are shared in L2.
-int pick_band(int64_t tiles_n, int units) {
+// Raster band (N-tiles swept before stepping along M).  The tiles that run at
+// once cover about units / band M-tiles of `band` N-tiles, a square-ish
+// footprint, so A rows and B columns are shared in L2 (band 4 for 76 pairs).
+// When A and B together do not fit in L2, A is read from DRAM once per band:
+// the band then widens while its B panels (bn columns x K each) take at most
+// kBandL2Bytes, so that they stay in L2 while A streams past and A is read
+// tiles_n / band times.  TG_BAND=<n> overrides the choice (tuning sweeps).
+constexpr int64_t kBandL2Bytes = int64_t(32) << 20;
+constexpr int64_t kOperandsInL2 = int64_t(96) << 20;
+
+int pick_band(int64_t tiles_n, int units, int bn, int64_t K, int64_t rows) {
     int band = 1;
     while (band * band * 2 <= units && band < 16) band *= 2;
+    const int64_t panel = static_cast<int64_t>(bn) * K * 2;
+    if ((rows + tiles_n * bn) * K * 2 > kOperandsInL2)
+        while (band < 16 && 2 * band * panel <= kBandL2Bytes && 2 * band <= tiles_n) band *= 2;
+    if (const char* env = std::getenv("TG_BAND")) {
+        const long b = std::strtol(env, nullptr, 10);
+        if (b >= 1 && b <= 64) band = static_cast<int>(b);
+    }
     if (band > tiles_n) band = static_cast<int>(tiles_n);
     return band < 1 ? 1 : band;
 }
@@ -372,11 +419,14 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     return TG_OK;
 }
 
-void base_params(Params* p, DeviceState* d) {
-    p->err = d->err;
+// Launch-wide fields every launch carries: the error record, the wait budget,
+// and the test and trace hooks armed on this thread (consumed by this launch).
+void base_params(Params* p, tg::ErrorRecord* err) {
+    p->err = err;
     p->wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
-    p->withhold_kb = t_withhold;
-    t_withhold = -1;
+    p->withhold_kb = t_withhold.kb;
+    p->withhold_block = t_withhold.block;
+    t_withhold = WithholdArm{};
     p->trace_tiles = t_trace.tiles;
     p->trace_tiles_cap = t_trace.tiles_cap;
     p->trace_ctas = t_trace.ctas;
@@ -384,11 +434,16 @@ void base_params(Params* p, DeviceState* d) {
     t_trace = TraceArm{};
 }
 
+// Launch with one CTA (pair) per work unit that has work: every resident unit,
+// or fewer when there are fewer whole tiles plus stream-K ranges than units.
 tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t stream) {
-    int64_t want = p.total_units < units ? p.total_units : units;
+    int64_t want = p.total_tiles - p.sk_tiles;
+    if (p.sk_units > want) want = p.sk_units;
+    if (want > units) want = units;
     const int grid = static_cast<int>(want) * v.cta_group;
     cudaError_t e = v.launch(p, grid, stream);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    ++t_launches;
     return TG_OK;
 }
 
@@ -402,78 +457,33 @@ tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t str
 // fail or stall on an allocation, or an application whose device memory is
 // owned by its own allocator under a fixed budget.  tg_grouped_gemm allocates a
 // small stream-ordered workspace per call for the problem table; this entry
-// point keeps the table in the fixed array below instead.  The array lives in
-// the library's device image, so every GPU that loads libtg holds it (128 KiB)
+// point keeps the table in g_noalloc_table instead.  The array lives in the
+// library's device image, so every GPU that loads libtg holds it (128 KiB)
 // until the process exits.  All calls share it: a call overwrites the entries
 // it uses, and a kernel reads only the entries its own call wrote, so nothing
 // has to start at zero; two calls whose copies and kernels overlap on the GPU
 // (different streams, no ordering between them) race on it.
 
-static __device__ __align__(256) tg::Problem g_noalloc_table[TG_NOALLOC_MAX_PROBLEMS];
-static_assert(sizeof(g_noalloc_table) == 128 * 1024, "the header states a 128 KiB table");
-
 namespace {
 
-struct NoallocDevice {
-    bool ready = false;
-    int sms = 0;
-    tg::ErrorRecord* err = nullptr;
-    tg::Problem* table = nullptr;   // device address of g_noalloc_table on this device
-    int units[128] = {};
-};
-
-NoallocDevice g_noalloc[kMaxDevices];
-
-// Once per device, with that device current: device checks and the device
-// addresses of the scratch table and the error record.  In host code the
-// array's name is only a stand-in for the symbol, so its address on this device
-// comes from cudaGetSymbolAddress.
-tg_status noalloc_device(NoallocDevice** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return fail(TG_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+// The device address of g_noalloc_table on d's device, looked up once per
+// device by the first no-alloc call (with that device current).  In host code
+// the array's name is only a stand-in for the symbol: a kernel given it would
+// read the wrong memory, so its address comes from cudaGetSymbolAddress.
+tg_status noalloc_table(DeviceState* d, tg::Problem** out) {
     std::lock_guard<std::mutex> lock(g_mu);
-    NoallocDevice& d = g_noalloc[dev];
-    if (!d.ready) {
-        int major = 0, minor = 0;
-        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return cuda_fail(e, "cudaDeviceGetAttribute");
-        if (major != 10 || minor != 3)
-            return fail(TG_ERR_UNSUPPORTED, "device %d is sm_%d%d; libtg is built for sm_103a (GB300) only", dev,
-                        major, minor);
-        void* sym = nullptr;
-        if ((e = cudaGetSymbolAddress(&sym, g_tg_error)) != cudaSuccess)
-            return cuda_fail(e, "cudaGetSymbolAddress(error record)");
-        d.err = static_cast<tg::ErrorRecord*>(sym);
+    if (!d->noalloc_table) {
         tg::Problem* tab = nullptr;
-        if ((e = cudaGetSymbolAddress((void**)&tab, g_noalloc_table)) != cudaSuccess)
-            return cuda_fail(e, "cudaGetSymbolAddress(no-alloc problem table)");
-        d.table = tab;
-        d.ready = true;
+        cudaError_t e = cudaGetSymbolAddress((void**)&tab, g_noalloc_table);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc problem table)");
+        d->noalloc_table = tab;
     }
-    *out = &d;
+    *out = d->noalloc_table;
     return TG_OK;
 }
 
-tg_status noalloc_resident(NoallocDevice* d, int vi, int* units) {
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (d->units[vi] > 0) { *units = d->units[vi]; return TG_OK; }
-    }
-    int u = 0;
-    cudaError_t e = kVariants[vi].units(&u);
-    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
-    if (u <= 0) return fail(TG_ERR_UNSUPPORTED, "kernel variant %d cannot be resident on this device", vi);
-    std::lock_guard<std::mutex> lock(g_mu);
-    d->units[vi] = u;
-    *units = u;
-    return TG_OK;
-}
-
-// Host staging for one call's table: fixed per-thread storage, no heap.
+// Host staging for one call's table: fixed per-thread storage, no heap.  The
+// next no-alloc call on the thread overwrites it.
 thread_local tg::Problem t_noalloc_host[TG_NOALLOC_MAX_PROBLEMS];
 
 }  // namespace
@@ -523,6 +533,7 @@ tg_status tg_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps
     if ((s = device_state(&d)) != TG_OK) return s;
     cudaError_t e = tg::launch_row_rms(A, lda, M, K, eps, r, d->sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "row statistics launch");
+    ++t_launches;
     return TG_OK;
 }
 
@@ -550,54 +561,18 @@ tg_status tg_gemm_ex(const tg_group_problem* problem, tg_stream_t stream) {
 
 namespace {
 
-// Split of the last, partial wave of a dense launch: its R tiles are cut into S
-// K-ranges (slices) so R * S work units spread over the resident CTAs (pairs).
-constexpr int kMinSliceKb = 4;    // k-blocks (of 64) per slice at least
-constexpr int kMaxSlices = 8;
-
-struct SplitPlan {
-    int64_t first = 0;   // first split tile
-    int tiles = 0;       // R
-    int slices = 0;      // S (0: no split)
-    bool nsplit = false; // column halves instead of K-ranges
-};
-
-// The last wave's R tiles: cut into two column halves when they then fit (2R units)
-// - a 256-wide tile's N = 128 MMAs take half the time and need no partial sums -
-// else into S K-ranges.
-SplitPlan plan_split(int64_t tiles, int units, int k_blocks, int bn) {
-    SplitPlan sp;
-    const char* env = std::getenv("TG_SPLIT_TAIL");
-    if (env && env[0] == '0') return sp;
-    if (units <= 0) return sp;
-    const int64_t R = tiles % units;
-    if (R == 0) return sp;
-    // Column halves still load the whole A box for half the MMA time; measured on GB300
-    // they beat K-ranges at 64 k-blocks (4096^3) and lose at 128 (8192^3), where the
-    // K-ranges' add-up costs relatively less.
-    if (bn == 256 && tiles > units && 2 * R <= units && k_blocks <= 96 && !(env && env[0] == 'k')) {
-        sp.first = tiles - R;
-        sp.tiles = static_cast<int>(R);
-        sp.slices = 2;
-        sp.nsplit = true;
-        return sp;
-    }
-    if (k_blocks < 2 * kMinSliceKb) return sp;
-    int64_t S = units / R;
-    if (S > k_blocks / kMinSliceKb) S = k_blocks / kMinSliceKb;
-    if (S > kMaxSlices) S = kMaxSlices;
-    if (S < 2) return sp;
-    sp.first = tiles - R;
-    sp.tiles = static_cast<int>(R);
-    sp.slices = static_cast<int>(S);
-    return sp;
+// Stream-K plan of a dense launch (tg::sk_plan); TG_STREAM_K=0 in the
+// environment turns it off (every tile in one piece, as grouped launches).
+tg::SkPlan plan_stream_k(int64_t tiles, int units, int k_blocks) {
+    const char* env = std::getenv("TG_STREAM_K");
+    if (env && env[0] == '0') return tg::SkPlan{};
+    return tg::sk_plan(tiles, units, k_blocks);
 }
 
 tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
-    const void* B = q.B;
     const tg_layout layout_a = q.la, layout_b = q.lb;
     const tg_dtype c_dtype = q.cd;
-    const int64_t ldb = q.ldb, M = q.M, N = q.N, K = q.K;
+    const int64_t M = q.M, N = q.N;
     tg_status s = check(q, 0);
     if (s != TG_OK) return s;
     if (M == 0 || N == 0) return TG_OK;
@@ -619,32 +594,28 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
     p.problems = nullptr;
     p.num_problems = 1;
     const int64_t tiles = static_cast<int64_t>(p.dense.tiles_m) * p.dense.tiles_n;
-    p.total_units = tiles;
-    p.band = pick_band(p.dense.tiles_n, units);
-    base_params(&p, d);
+    p.total_tiles = tiles;
+    p.band = pick_band(p.dense.tiles_n, units, v.bn, q.K, q.M);
+    base_params(&p, d->err);
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const SplitPlan sp = plan_split(tiles, units, p.dense.k_blocks, v.bn);
+    const tg::SkPlan sp = plan_stream_k(tiles, units, p.dense.k_blocks);
     void* ws = nullptr;
     int n_counters = 0;
-    if (sp.nsplit) {
-        p.sk_first = sp.first;
-        p.sk_tiles = sp.tiles;
-        p.sk_slices = 2;
-        p.sk_nsplit = 1;
-        p.total_units = sp.first + 2 * static_cast<int64_t>(sp.tiles);
-    } else if (sp.slices > 1) {
-        // partial sums of every slice, then one arrival counter per (split tile, CTA, epilogue warp)
-        const size_t partial = static_cast<size_t>(sp.tiles) * sp.slices * v.tile_m * v.bn * sizeof(float);
+    if (sp.tiles > 0) {
+        // partial sums of every piece, then one arrival counter per (tile, CTA, epilogue warp)
+        const size_t partial =
+            static_cast<size_t>(sp.tiles) * sp.max_slices * v.tile_m * v.bn * sizeof(float);
         n_counters = sp.tiles * v.cta_group * tg::NUM_EPI_WARPS;
-        cudaError_t e = cudaMallocFromPoolAsync(&ws, partial + n_counters * sizeof(uint32_t), d->pool, st);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(split partials)");
-        p.sk_first = sp.first;
+        cudaMemPool_t pool = nullptr;
+        if ((s = device_pool(d, &pool)) != TG_OK) return s;
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, partial + n_counters * sizeof(uint32_t), pool, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(stream-K partials)");
         p.sk_tiles = sp.tiles;
-        p.sk_slices = sp.slices;
+        p.sk_units = sp.units;
+        p.sk_max_slices = sp.max_slices;
         p.sk_partial = static_cast<float*>(ws);
         p.sk_count = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + partial);
-        p.total_units = sp.first + static_cast<int64_t>(sp.tiles) * sp.slices;
     }
     // the kernel before the GEMM: the row pass (which also zeroes the counters) or the counter reset;
     // the GEMM follows it as a programmatic dependent and waits for it only where it reads its output
@@ -653,11 +624,12 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
                                     n_counters);
     else if (n_counters) e = tg::launch_clear_counters(p.sk_count, n_counters, st);
     s = e == cudaSuccess ? TG_OK : cuda_fail(e, pre ? "row statistics launch" : "counter reset launch");
+    if (s == TG_OK && (pre || n_counters)) ++t_launches;
     p.pdl = (pre != nullptr || n_counters > 0) ? 1 : 0;
     if (s == TG_OK) s = enqueue(p, v, units, st);
     if (ws) {
         e = cudaFreeAsync(ws, st);   // stream-ordered: released after the GEMM has run
-        if (e != cudaSuccess && s == TG_OK) s = cuda_fail(e, "cudaFreeAsync(split partials)");
+        if (e != cudaSuccess && s == TG_OK) s = cuda_fail(e, "cudaFreeAsync(stream-K partials)");
     }
     return s;
 }
@@ -709,9 +681,9 @@ tg_status tg_gemm_bcast(const void* A_user, tg_layout layout_a, int64_t lda, int
     p.dense.replicas = static_cast<int32_t>(replicas);
     p.dense.tile_begin = 0;
     p.num_problems = 1;
-    p.total_units = tiles * replicas;
-    p.band = pick_band(p.dense.tiles_n, units);
-    base_params(&p, d);
+    p.total_tiles = tiles * replicas;
+    p.band = pick_band(p.dense.tiles_n, units, v.bn, K, U);
+    base_params(&p, d->err);
     return enqueue(p, v, units, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -727,7 +699,6 @@ tg_status tg_moe_gemm(const void* A, int64_t lda, int64_t T, int64_t K, const vo
                     TG_MOE_MAX_EXPERTS);
     if (!counts) return fail(TG_ERR_INVALID_ARG, "counts is NULL");
     if (reinterpret_cast<uintptr_t>(counts) & 3u) return fail(TG_ERR_INVALID_ARG, "counts is not 4-byte aligned");
-    if (N % 8) return fail(TG_ERR_UNSUPPORTED, "N=%lld must be a multiple of 8 in the device-counts form", (long long)N);
     const Prob q{A, TG_ROW_MAJOR, lda, B, layout_b, ldb, C, c_dtype, ldc, T, N, K, epi, bias, TG_BF16};
     tg_status s = check(q, 0);
     if (s != TG_OK) return s;
@@ -773,18 +744,37 @@ tg_status tg_moe_gemm(const void* A, int64_t lda, int64_t T, int64_t K, const vo
         if (s != TG_OK) return s;
     }
     p.num_problems = 1;
-    p.total_units = 0;   // the kernel derives it from the device counts
-    p.band = pick_band(p.dense.tiles_n, units);
+    p.total_tiles = 0;   // the kernel derives it from the device counts
+    p.band = pick_band(p.dense.tiles_n, units, v.bn, 0, 0);
     p.moe_counts = counts;
     p.moe_groups = static_cast<int32_t>(G);
     p.moe_rows = T;
-    p.moe_c = C;
-    p.moe_ldc = ldc;
-    base_params(&p, d);
-    const int grid = units * v.cta_group;
-    cudaError_t e = v.launch(p, grid, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
-    return TG_OK;
+    base_params(&p, d->err);
+
+    // Each expert's own A and C maps, written on the device from the counts by a small
+    // kernel that the GEMM follows as a programmatic dependent (stream-ordered workspace).
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaMemPool_t pool = nullptr;
+    if ((s = device_pool(d, &pool)) != TG_OK) return s;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, static_cast<size_t>(2 * G) * sizeof(CUtensorMap), pool, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(per-expert tensor maps)");
+    p.moe_maps = static_cast<const CUtensorMap*>(ws);
+    const int64_t c_esize = c_dtype == TG_F32 ? 4 : 2;
+    e = tg::launch_moe_maps(p.dense.tma_a, p.dense.tma_c, counts, static_cast<int>(G), A, lda * 2, C, ldc * c_esize, T,
+                            static_cast<CUtensorMap*>(ws), st);
+    s = e == cudaSuccess ? TG_OK : cuda_fail(e, "per-expert tensor map launch");
+    if (s == TG_OK) {
+        ++t_launches;
+        p.pdl = 1;
+        const int grid = units * v.cta_group;
+        e = v.launch(p, grid, st);
+        if (e != cudaSuccess) s = cuda_fail(e, "kernel launch");
+        else ++t_launches;
+    }
+    e = cudaFreeAsync(ws, st);   // stream-ordered: released after the GEMM has run
+    if (e != cudaSuccess && s == TG_OK) s = cuda_fail(e, "cudaFreeAsync(per-expert tensor maps)");
+    return s;
 }
 
 tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stream) {
@@ -805,6 +795,8 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
     tg_status s;
     if ((s = device_state(&d)) != TG_OK) return s;
     if ((s = encoder()) != TG_OK) return s;
+    cudaMemPool_t pool = nullptr;
+    if ((s = device_pool(d, &pool)) != TG_OK) return s;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     // One launch per (layout_a, layout_b, c_dtype) class, classes in order of first appearance.
@@ -817,7 +809,7 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
         if (it == classes.end()) { order.push_back(key); classes[key] = {g}; }
         else it->second.push_back(g);
     }
-    const int64_t withhold = t_withhold;
+    const WithholdArm withhold = t_withhold;
     for (const auto& key : order) {
         const std::vector<int>& members = classes[key];
         int64_t max_n = 0, rows = 0;
@@ -842,7 +834,7 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
         }
         const size_t bytes = host.size() * sizeof(Problem);
         void* ws = nullptr;
-        cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, d->pool, st);
+        cudaError_t e = cudaMallocFromPoolAsync(&ws, bytes, pool, st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync(problem table)");
         e = cudaMemcpyAsync(ws, host.data(), bytes, cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) {
@@ -853,16 +845,16 @@ tg_status tg_grouped_gemm(const tg_group_problem* table, int G, tg_stream_t stre
         std::memset(&p, 0, sizeof p);
         p.problems = static_cast<const Problem*>(ws);
         p.num_problems = static_cast<int32_t>(host.size());
-        p.total_units = tiles;
-        p.band = pick_band(max_tiles_n, units);
+        p.total_tiles = tiles;
+        p.band = pick_band(max_tiles_n, units, v.bn, 0, 0);
         t_withhold = withhold;
-        base_params(&p, d);
+        base_params(&p, d->err);
         s = enqueue(p, v, units, st);
         e = cudaFreeAsync(ws, st);
         if (s != TG_OK) return s;
         if (e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(problem table)");
     }
-    t_withhold = -1;
+    t_withhold = WithholdArm{};
     return TG_OK;
 }
 
@@ -883,24 +875,40 @@ tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_strea
         return fail(TG_ERR_UNSUPPORTED,
                     "%d non-empty problems, but the fixed no-alloc table holds at most %d; split the call or use "
                     "tg_grouped_gemm", live, TG_NOALLOC_MAX_PROBLEMS);
-    NoallocDevice* d = nullptr;
-    tg_status s;
-    if ((s = noalloc_device(&d)) != TG_OK) return s;
-    if ((s = encoder()) != TG_OK) return s;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // The descriptors travel from t_noalloc_host, which the thread's next call
+    // overwrites: a captured copy would read it again at replay, so a stream
+    // under capture is refused before anything is enqueued.
+    cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(st, &capturing);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+    if (capturing != cudaStreamCaptureStatusNone)
+        return fail(TG_ERR_UNSUPPORTED,
+                    "tg_grouped_gemm_noalloc does not run on a stream that is being captured (its descriptor copy "
+                    "reads a host buffer that the next call overwrites)");
+    DeviceState* d = nullptr;
+    tg_status s;
+    if ((s = device_state(&d)) != TG_OK) return s;
+    tg::Problem* dev_table = nullptr;
+    if ((s = noalloc_table(d, &dev_table)) != TG_OK) return s;
+    if ((s = encoder()) != TG_OK) return s;
 
     // Classes (layout_a, layout_b, c_dtype) in order of first appearance; each
     // class gets its own consecutive slice of the table and its own launch.
+    auto class_of = [](const tg_group_problem& t) {
+        return (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) +
+               (t.c_dtype == TG_F32 ? 1 : 0);
+    };
     int class_order[8], n_classes = 0;
     for (int g = 0; g < G; ++g) {
         const tg_group_problem& t = table[g];
         if (t.M == 0 || t.N == 0) continue;
-        const int key = (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) + (t.c_dtype == TG_F32 ? 1 : 0);
+        const int key = class_of(t);
         bool seen = false;
         for (int c = 0; c < n_classes; ++c) seen = seen || class_order[c] == key;
         if (!seen) class_order[n_classes++] = key;
     }
-    const int64_t withhold = t_withhold;
+    const WithholdArm withhold = t_withhold;
     int offset = 0;
     for (int c = 0; c < n_classes; ++c) {
         const int key = class_order[c];
@@ -908,9 +916,7 @@ tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_strea
         int64_t max_n = 0, rows = 0;
         for (int g = 0; g < G; ++g) {
             const tg_group_problem& t = table[g];
-            if (t.M == 0 || t.N == 0) continue;
-            const int k2 = (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) + (t.c_dtype == TG_F32 ? 1 : 0);
-            if (k2 != key) continue;
+            if (t.M == 0 || t.N == 0 || class_of(t) != key) continue;
             max_n = t.N > max_n ? t.N : max_n;
             rows += t.M;
         }
@@ -918,16 +924,14 @@ tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_strea
         const int vi = variant_index(true, f32, tc.cta_group, tc.bn, a_col, !b_col);
         const Variant& v = kVariants[vi];
         int units = 0;
-        if ((s = noalloc_resident(d, vi, &units)) != TG_OK) return s;
+        if ((s = resident(d, vi, &units)) != TG_OK) return s;
 
         tg::Problem* host = t_noalloc_host + offset;
         int n = 0;
         int64_t tiles = 0, max_tiles_n = 1;
         for (int g = 0; g < G; ++g) {
             const tg_group_problem& t = table[g];
-            if (t.M == 0 || t.N == 0) continue;
-            const int k2 = (t.layout_a == TG_COL_MAJOR ? 4 : 0) + (t.layout_b == TG_COL_MAJOR ? 2 : 0) + (t.c_dtype == TG_F32 ? 1 : 0);
-            if (k2 != key) continue;
+            if (t.M == 0 || t.N == 0 || class_of(t) != key) continue;
             const Prob q = prob_of(t);
             if ((s = fill_problem(q, v, g, &host[n])) != TG_OK) return s;
             host[n].tile_begin = tiles;
@@ -935,21 +939,20 @@ tg_status tg_grouped_gemm_noalloc(const tg_group_problem* table, int G, tg_strea
             if (host[n].tiles_n > max_tiles_n) max_tiles_n = host[n].tiles_n;
             ++n;
         }
-        cudaError_t e = cudaMemcpyAsync(d->table + offset, host, n * sizeof(tg::Problem), cudaMemcpyHostToDevice, st);
+        cudaError_t e = cudaMemcpyAsync(dev_table + offset, host, n * sizeof(tg::Problem), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(no-alloc problem table)");
         Params p;
         std::memset(&p, 0, sizeof p);
-        p.problems = d->table + offset;
+        p.problems = dev_table + offset;
         p.num_problems = n;
-        p.total_units = tiles;
-        p.band = pick_band(max_tiles_n, units);
-        p.err = d->err;
-        p.wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
-        p.withhold_kb = withhold;
+        p.total_tiles = tiles;
+        p.band = pick_band(max_tiles_n, units, v.bn, 0, 0);
+        t_withhold = withhold;
+        base_params(&p, d->err);
         if ((s = enqueue(p, v, units, st)) != TG_OK) return s;
         offset += n;
     }
-    t_withhold = -1;
+    t_withhold = WithholdArm{};
     return TG_OK;
 }
 
@@ -985,10 +988,12 @@ tg_status tg_device_status(tg_stream_t stream) {
         return fail(TG_ERR_INVALID_ARG,
                     "device token counts are negative or sum to %lld rows, more than T; the launch computed nothing",
                     (long long)rec.tile);
-    static const char* roles[] = {"?", "TMA producer", "MMA issuer", "epilogue", "MMA drain"};
-    return fail(TG_ERR_TIMEOUT, "in-kernel wait ran out: role=%s block=%u stage=%u tile=%lld waited=%.1f ms",
+    static const char* roles[] = {"?", "TMA producer", "MMA issuer", "epilogue", "abort drain"};
+    return fail(TG_ERR_TIMEOUT,
+                "in-kernel wait ran out: role=%s block=%u stage=%u slot=%lld waited=%.1f ms; %u abort-path "
+                "drains ran out",
                 rec.role < 5 ? roles[rec.role] : "?", rec.block, rec.stage, (long long)rec.tile,
-                rec.waited_ns / 1e6);
+                rec.waited_ns / 1e6, rec.drains);
 }
 
 tg_status tg_set_wait_budget_ms(uint32_t ms) {
@@ -997,11 +1002,14 @@ tg_status tg_set_wait_budget_ms(uint32_t ms) {
     return TG_OK;
 }
 
-tg_status tg_debug_withhold_stage(int64_t k_block) {
+tg_status tg_debug_withhold_stage_in(int64_t k_block, int32_t block) {
     if (k_block < -1) return fail(TG_ERR_INVALID_ARG, "k_block must be >= -1");
-    t_withhold = k_block;
+    if (block < 0) return fail(TG_ERR_INVALID_ARG, "block must be >= 0");
+    t_withhold = WithholdArm{k_block, block};
     return TG_OK;
 }
+
+tg_status tg_debug_withhold_stage(int64_t k_block) { return tg_debug_withhold_stage_in(k_block, 0); }
 
 tg_status tg_debug_trace(uint64_t* tile_records, int64_t tile_capacity, uint64_t* cta_records, int64_t cta_capacity) {
     if (tile_capacity < 0 || cta_capacity < 0) return fail(TG_ERR_INVALID_ARG, "negative trace capacity");
@@ -1012,6 +1020,8 @@ tg_status tg_debug_trace(uint64_t* tile_records, int64_t tile_capacity, uint64_t
     return TG_OK;
 }
 
-uint32_t tg_version(void) { return (0u << 16) | 1u; }
+uint32_t tg_version(void) { return (0u << 16) | 2u; }
+
+uint64_t tg_launch_count(void) { return t_launches; }
 
 }  // extern "C"

@@ -23,19 +23,26 @@
 // tcgen05.mma.cta_group::2 over both, and each CTA's TMEM receives its 128
 // rows of the accumulator.  No TMA multicast is used.
 //
-// The tile scheduler is static and persistent: CTA (pair) i takes work units
-// i, i + U, i + 2U, ... of the concatenated tile list of all problems; within a
-// problem tiles are rastered in bands of `band` N-tiles so that concurrently
-// running tiles share A rows and B columns in L2.  A work unit is a tile,
-// except in a dense launch's last, partial wave, whose tiles are split into
-// column halves or K-ranges (Params::sk_*).  In grouped and MoE launches a
-// problem's last M-tile with at most 128 rows is a half tile (M = 128 MMAs).
+// The tile scheduler is static and persistent.  CTA (pair) u of U takes whole
+// tiles u, u + U, u + 2U, ... of the concatenated tile list of all problems;
+// within a problem tiles are rastered in bands of `band` N-tiles so that
+// concurrently running tiles share A rows and B columns in L2.  A dense launch
+// whose tiles do not divide evenly over the U units is balanced with stream-K:
+// the k-blocks of its first R tiles (R = tiles mod U, or all tiles when there
+// are fewer than U) are cut into equal contiguous ranges, one per unit, and
+// every unit runs its range (one or two tile pieces) before its whole tiles.
+// Each piece writes its fp32 partial sums to a workspace; the piece that
+// arrives last adds all of them in k order and runs the epilogue, while the
+// unit's MMA issuer is already on its next tile.  In grouped and MoE launches
+// a problem's last M-tile with at most 128 rows is a half tile (M = 128 MMAs).
 //
 // Every mbarrier wait is bounded (wait_budget_ns, measured with %globaltimer).
 // On expiry the waiting thread records the failure in the device error
 // record, raises the CTA's abort flag (and its peer's), and all roles leave
-// their loops: in-flight TMA loads are waited for, issued MMAs are drained
-// with a final commit, tensor memory is freed and the kernel returns.
+// their loops: the producer waits until the TMA loads it issued have landed
+// (in a pair, the leader closes the phases the other CTA left open and waits
+// for both CTAs' loads), issued MMAs are drained with a final commit, tensor
+// memory is freed and the kernel returns.
 #pragma once
 
 #include <cuda.h>
@@ -54,10 +61,12 @@ constexpr int UMMA_K = 16;           // K per tcgen05.mma.kind::f16
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;         // warps 2..5 drain TMEM; warp w reads lanes 32*(w%4)..+31
 constexpr int NUM_EPI_WARPS = 4;
-constexpr int FIX_BUFS = 4;          // chunks in flight per warp while adding up a split tile
+constexpr int FIX_BUFS = 4;          // chunks in flight per warp while a unit's last piece adds up its tile
 constexpr int C_STAGE_BYTES = 32 * 128;   // per-warp store staging buffer: 32 rows x 128 bytes
 constexpr int SMEM_LIMIT = 232448;        // max dynamic shared memory per CTA on sm_100 family
 constexpr int MOE_MAX_G = 190;            // experts per call of the device-counts MoE form (table in shared memory)
+constexpr int SK_QUANTUM = 4;             // stream-K range boundaries fall on multiples of 4 k-blocks
+constexpr int MAX_STAGES = 8;
 
 enum : uint32_t { ERR_NONE = 0, ERR_TIMEOUT = 1, ERR_COUNTS = 2 };
 enum : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_DRAIN = 4 };
@@ -68,8 +77,10 @@ struct ErrorRecord {
     uint32_t role;        // ROLE_*
     uint32_t block;       // blockIdx.x of the reporting CTA
     uint32_t stage;       // ring stage or accumulator buffer being waited on
-    int64_t tile;         // global tile index
+    int64_t tile;         // work item slot
     uint64_t waited_ns;
+    uint32_t drains;      // waits of the abort path (issued loads, issued MMAs) that ran out too
+    uint32_t pad;
 };
 
 // One GEMM problem as the device sees it.
@@ -104,44 +115,132 @@ struct Params {
     const Problem* problems;    // grouped launch: device array written by the host
     int32_t num_problems;
     int32_t band;               // raster band width in N-tiles
-    int64_t total_units;        // work units: whole tiles, plus one per extra slice of a split tile
+    int64_t total_tiles;        // tiles of the launch (dense broadcast form: tiles x replicas)
     ErrorRecord* err;
     uint64_t wait_budget_ns;
-    int64_t withhold_kb;        // test hook, -1 = off (see tg_debug_withhold_stage)
-    // Timeline trace (tg_debug_trace), null when off.  trace_tiles[t] = {block,
-    // first k-block ready, accumulator complete, epilogue done} for global tile
-    // t < trace_tiles_cap (times from %globaltimer, ns); trace_ctas[b] =
-    // {set-up done, teardown start} for block b < trace_ctas_cap.
+    int64_t withhold_kb;        // test hook, -1 = off (see tg_debug_withhold_stage_in)
+    int32_t withhold_block;
+    // Timeline trace (tg_debug_trace), null when off.  trace_tiles[s] = {block,
+    // first k-block ready, accumulator complete, epilogue done} for work item slot
+    // s < trace_tiles_cap, where the i-th item of unit u has slot i * U + u (times
+    // from %globaltimer, ns); trace_ctas[b] = {entry, set-up done, teardown start,
+    // exit} for block b < trace_ctas_cap.
     uint64_t* trace_tiles;
     int64_t trace_tiles_cap;
     uint64_t* trace_ctas;
     int64_t trace_ctas_cap;
     // Device-counts MoE form: expert g owns rows [off_g, off_g + moe_counts[g]) of A and C,
     // off_g = sum of the counts before g; B is a 3-D map [G][K][N] (or [G][N][K]).
+    // moe_maps[2 g] and [2 g + 1] are expert g's own A and C maps (its moe_counts[g] rows),
+    // written on the device by the kernel launched just before this one (moe_maps_kernel).
     const int32_t* moe_counts;
     int32_t moe_groups;
     int64_t moe_rows;           // T: rows of A and C; the counts must sum to at most T
-    void* moe_c;                // C base pointer, for rows stored without TMA
-    int64_t moe_ldc;            // elements per row of C
+    const CUtensorMap* moe_maps;
     // Host side only: launch as a programmatic dependent of the kernel before it in the
-    // stream (the row-statistics pass of the fused RMS norm).  Only the epilogue reads
-    // that kernel's output, after griddepcontrol.wait; set-up and main loop overlap it.
+    // stream (the row-statistics pass of the fused RMS norm, or the counter reset).
+    // Only the reads of that kernel's output wait for it (griddepcontrol.wait); set-up
+    // and main loop overlap it.
     int32_t pdl;
-    // Split tiles (dense only).  Tiles [sk_first, sk_first + sk_tiles) - the last,
-    // partial wave of the persistent schedule - are each computed by sk_slices work
-    // units over consecutive K-ranges, run by different CTAs (pairs) at the same time.
-    // Every slice writes its fp32 partial sums to sk_partial; the slice that arrives
-    // last at sk_count (zeroed by the kernel launched just before) adds the partials
-    // in slice order and runs the epilogue, so results do not depend on timing.
-    int64_t sk_first;
-    int32_t sk_tiles;
-    int32_t sk_slices;          // 0: no split
-    // 1: the split tiles are cut into two column halves instead (BN/2-wide MMAs take
-    // half the time; no partial sums): units sk_first + h * sk_tiles + j, h = 0, 1.
-    int32_t sk_nsplit;
-    float* sk_partial;          // [sk_tiles][sk_slices][CTA_GROUP][4 warps][BN/4][32 lanes][4]
-    uint32_t* sk_count;         // [sk_tiles][CTA_GROUP][4 warps]
+    // Stream-K (dense only; see the file header).  The sk_tiles * k_blocks k-blocks of
+    // tiles [0, sk_tiles), in tile order, are cut into sk_units contiguous ranges, range
+    // r = [sk_bound(r), sk_bound(r + 1)) belonging to unit r.  Tiles [sk_tiles,
+    // total_tiles) are whole tiles: unit u takes sk_tiles + u, sk_tiles + u + U, ...
+    int32_t sk_tiles;           // 0: no stream-K
+    int32_t sk_units;
+    int32_t sk_max_slices;      // pieces of one tile at most (stride of the partial slabs)
+    float* sk_partial;          // [sk_tiles][sk_max_slices][CTA_GROUP][4 warps][BN/4][32 lanes][4]
+    uint32_t* sk_count;         // [sk_tiles][CTA_GROUP][4 warps], zero at launch
 };
+
+// ----------------------------------------------------------------------------------------
+// stream-K ranges (shared by the host plan and the kernel)
+
+// First k-block of unit r's range in the stream-K space of `total` k-blocks:
+// SK_QUANTUM * floor(r * G / units) with G = floor(total / SK_QUANTUM); the last
+// range ends at `total`.  Ranges are non-empty when G >= units.
+__host__ __device__ __forceinline__ int64_t sk_bound(int64_t r, int64_t units, int64_t total) {
+    if (r >= units) return total;
+    const int64_t G = total / SK_QUANTUM;
+    return SK_QUANTUM * ((r * G) / units);
+}
+
+// The unit whose range holds k-block x: the largest r with sk_bound(r) <= x.
+__host__ __device__ __forceinline__ int64_t sk_owner(int64_t x, int64_t units, int64_t total) {
+    const int64_t G = total / SK_QUANTUM;
+    const int64_t X = x / SK_QUANTUM;
+    const int64_t r = ((X + 1) * units + G - 1) / G - 1;
+    return r < units - 1 ? r : units - 1;
+}
+
+// One piece of a stream-K range: k-blocks [kb0, kb1) of tile t, the slice-th of
+// the tile's `slices` pieces in k order (slices == 0: the range holds the whole
+// tile, which then needs no partial sums).
+struct SkPiece {
+    int64_t t;
+    int kb0, kb1;
+    int slice, slices;
+};
+
+// The piece that starts at k-block `cur` of unit `unit`'s range [.., end), in the
+// stream-K space of `total` = tiles * k_blocks k-blocks cut into `units` ranges.
+__host__ __device__ __forceinline__ SkPiece sk_piece(int64_t cur, int64_t end, int k_blocks, int64_t units,
+                                                     int64_t total, int64_t unit) {
+    SkPiece q;
+    q.t = cur / k_blocks;
+    q.kb0 = static_cast<int>(cur - q.t * k_blocks);
+    const int64_t kb1 = q.kb0 + (end - cur);
+    q.kb1 = static_cast<int>(kb1 < k_blocks ? kb1 : k_blocks);
+    const int64_t first = sk_owner(q.t * k_blocks, units, total);
+    const int64_t last = sk_owner((q.t + 1) * k_blocks - 1, units, total);
+    q.slice = static_cast<int>(unit - first);
+    q.slices = last > first ? static_cast<int>(last - first + 1) : 0;
+    return q;
+}
+
+// Stream-K plan of a dense launch of `tiles` tiles of `k_blocks` k-blocks on
+// `units` resident units.  The R = tiles mod units tiles of the last, partial
+// wave (all tiles when there are fewer than units) would leave units - R units
+// idle while they run; instead their R * k_blocks k-blocks are cut into U
+// ranges (U = units, fewer where ranges would drop below SK_QUANTUM k-blocks or
+// a tile would be cut into more pieces than allowed: SK_MAX_PIECES when every
+// tile is in pieces, SK_MAX_PIECES_WITH_WHOLE when units also run whole tiles,
+// so that a tile's last piece reads back one or two partials only, while its
+// unit is busy with its next tile).  A piece costs a write of its fp32 partial
+// sums, so there is no stream-K when the pieces would be almost whole tiles
+// (R > 3 units / 4), when a range would hold a whole tile (U <= R), or when
+// k_blocks < 2 * SK_QUANTUM.
+constexpr int SK_MAX_PIECES = 8;
+constexpr int SK_MAX_PIECES_WITH_WHOLE = 2;
+
+struct SkPlan {
+    int tiles = 0;        // R: tiles [0, R) run as stream-K pieces (0: no stream-K)
+    int units = 0;        // U: units that own a range
+    int max_slices = 0;   // pieces of one tile at most
+};
+
+__host__ __forceinline__ SkPlan sk_plan(int64_t tiles, int64_t units, int64_t k_blocks) {
+    SkPlan sp;
+    if (units <= 1 || k_blocks < 2 * SK_QUANTUM || tiles <= 0) return sp;
+    const int64_t R = tiles < units ? tiles : tiles % units;
+    if (R == 0) return sp;
+    if (tiles > units && R * 4 > units * 3) return sp;
+    const int64_t total = R * k_blocks;
+    int64_t U = units;
+    const int64_t max_pieces = tiles > units ? SK_MAX_PIECES_WITH_WHOLE : SK_MAX_PIECES;
+    if (U > max_pieces * R) U = max_pieces * R;
+    if (U > total / SK_QUANTUM) U = total / SK_QUANTUM;
+    if (U <= R) return sp;
+    int64_t max_slices = 1;
+    for (int64_t t = 0; t < R; ++t) {
+        const int64_t n = sk_owner((t + 1) * k_blocks - 1, U, total) - sk_owner(t * k_blocks, U, total) + 1;
+        if (n > max_slices) max_slices = n;
+    }
+    sp.tiles = static_cast<int>(R);
+    sp.units = static_cast<int>(U);
+    sp.max_slices = static_cast<int>(max_slices);
+    return sp;
+}
 
 // MODE: 0 dense (tensor maps in parameter space), 1 grouped (problem table in
 // device memory), 2 MoE with device-resident token counts.
@@ -165,7 +264,7 @@ struct Config {
     static constexpr int MOE_BYTES = MOE ? 8 * (MOE_MAX_G + 1) : 0;   // tile and row prefix sums
     static constexpr int FIXED = C_BYTES + MOE_BYTES + 512 /*barriers and slots*/ + 1024 /*alignment slack*/;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -177,7 +276,14 @@ struct Config {
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static constexpr int OFF_MOE_TOTAL = OFF_ABORT + 4;
-    static constexpr int SMEM_BYTES = OFF_MOE_TOTAL + 4 + 1024;
+    // The producer's record of its ring, read after an abort (by the pair's leader
+    // through distributed shared memory): flag (set when final), ring positions
+    // advanced, and per stage the last position loaded there and its bytes.
+    static constexpr int OFF_DRAIN_FLAG = OFF_MOE_TOTAL + 4;
+    static constexpr int OFF_DRAIN_POS = OFF_DRAIN_FLAG + 4;
+    static constexpr int OFF_DRAIN_LAST = OFF_DRAIN_POS + 4;
+    static constexpr int OFF_DRAIN_BYTES = OFF_DRAIN_LAST + 4 * MAX_STAGES;
+    static constexpr int SMEM_BYTES = OFF_DRAIN_BYTES + 4 * MAX_STAGES + 1024;
 
 
     static_assert(BN == 128 || BN == 256, "tile width");
@@ -188,7 +294,7 @@ struct Config {
     static_assert(BN_CTA % 64 == 0, "MN-major B is loaded in 64-column boxes");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of two");
     static_assert(NUM_EPI_WARPS * FIX_BUFS * 32 * CW * 4 <= STAGES * STAGE_BYTES,
-                  "split-tile staging must fit in the operand ring");
+                  "the add-up staging of a unit's last piece must fit in the operand ring");
 };
 
 // ----------------------------------------------------------------------------------------
@@ -206,9 +312,6 @@ struct TileCoord {
     // columns [0, BN/2) in TMEM lanes 0-63 and [BN/2, BN) in lanes 64-127, both in
     // TMEM columns [0, BN/2).
     bool half;
-    // N-split unit (dense): columns [n0, n0 + BN/2) only, by MMAs of N = BN/2; the
-    // accumulator holds them in TMEM columns [0, BN/2) with the usual row layout.
-    bool nhalf;
 };
 
 // Device-counts MoE schedule, built in shared memory by every CTA at start:
@@ -264,7 +367,6 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     TileCoord c;
     c.g = g;
     c.half = false;
-    c.nhalf = false;
     if constexpr (Cfg::CTA_GROUP == 2 && (Cfg::GROUPED || Cfg::MOE)) {
         const int rows_left = (Cfg::MOE ? mt.row_off[g + 1] - mt.row_off[g] : pr.M) - mb * Cfg::TILE_M;
         c.half = rows_left <= BM;
@@ -280,46 +382,74 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     return c;
 }
 
-// A work unit: a whole tile, or one K-range (slice) of a split tile.
+// A work item: a whole tile, or one stream-K piece (a k-block range) of a tile.
 struct Work {
     int64_t t;    // tile
-    int kb0;      // split tiles: k-blocks [kb0, kb1); whole tiles use the problem's k_blocks
+    int kb0;      // k-blocks [kb0, kb1) of the tile; a whole tile uses its problem's k_blocks
     int kb1;
-    int slice;
-    int tail;     // index among the K-split tiles, or -1 for a whole tile
-    int nh;       // column half (0 or 1) of an N-split tile, or -1 for the whole width
+    int slice;    // piece: its index among the tile's pieces (k order)
+    int slices;   // piece: pieces of the tile (>= 2); 0 for a whole tile
+    int64_t slot; // i * U + u for the i-th item of unit u (trace index)
+};
+
+// The work items of one unit, in order: its first whole tile, its stream-K range
+// (one or two pieces), then its other whole tiles.  The first whole tiles of all
+// units start together on neighbouring tiles, which share their operands in L2;
+// a piece's partial sums are added up while the unit works on its next tile.
+struct Sched {
+    int64_t cur, end;    // rest of the unit's stream-K range (k-blocks of the stream-K space)
+    int64_t next_tile;   // its next whole tile
+    int64_t i;           // items handed out so far
 };
 
 template <class Cfg>
-__device__ __forceinline__ Work work_of(const Params& p, int64_t u) {
-    Work w{u, 0, 0, 0, -1, -1};
+__device__ __forceinline__ Sched sched_begin(const Params& p, int64_t unit) {
+    Sched s{0, 0, unit, 0};
     if constexpr (!Cfg::GROUPED && !Cfg::MOE) {
-        if (p.sk_nsplit && u >= p.sk_first) {
-            const int64_t v = u - p.sk_first;
-            w.t = p.sk_first + v % p.sk_tiles;
-            w.nh = static_cast<int>(v / p.sk_tiles);
-        } else if (p.sk_slices > 1 && u >= p.sk_first) {
-            const int64_t v = u - p.sk_first;
-            const int S = p.sk_slices;
-            const int kbs = p.dense.k_blocks;
-            w.tail = static_cast<int>(v % p.sk_tiles);
-            w.slice = static_cast<int>(v / p.sk_tiles);
-            w.t = p.sk_first + w.tail;
-            w.kb0 = static_cast<int>(static_cast<int64_t>(w.slice) * kbs / S);
-            w.kb1 = static_cast<int>(static_cast<int64_t>(w.slice + 1) * kbs / S);
+        if (p.sk_tiles > 0) {
+            const int64_t total = static_cast<int64_t>(p.sk_tiles) * p.dense.k_blocks;
+            if (unit < p.sk_units) {
+                s.cur = sk_bound(unit, p.sk_units, total);
+                s.end = sk_bound(unit + 1, p.sk_units, total);
+            }
+            s.next_tile = p.sk_tiles + unit;
         }
     }
-    return w;
+    return s;
 }
 
-// Coordinates of a work unit: its tile's, narrowed to one column half for N-split units.
 template <class Cfg>
-__device__ __forceinline__ TileCoord coord_of(const Params& p, const Work& w, int g, uint32_t rank,
-                                              const MoeTable& mt = {}) {
-    TileCoord c = tile_coord<Cfg>(p, w.t, g, rank, mt);
-    c.nhalf = w.nh >= 0;
-    if (c.nhalf) c.n0 += w.nh * (Cfg::BN / 2);
-    return c;
+__device__ __forceinline__ bool sched_next(const Params& p, int64_t unit, int64_t num_units, int64_t total_tiles,
+                                           Sched& s, Work& w) {
+    w.slot = s.i * num_units + unit;
+    if constexpr (!Cfg::GROUPED && !Cfg::MOE) {
+        if (s.cur < s.end && (s.i > 0 || s.next_tile >= total_tiles)) {
+            const int kbs = p.dense.k_blocks;
+            const SkPiece q = sk_piece(s.cur, s.end, kbs, p.sk_units, static_cast<int64_t>(p.sk_tiles) * kbs, unit);
+            w.t = q.t;
+            w.kb0 = q.kb0;
+            w.kb1 = q.kb1;
+            w.slice = q.slice;
+            w.slices = q.slices;
+            s.cur += q.kb1 - q.kb0;
+            ++s.i;
+            return true;
+        }
+    }
+    if (s.next_tile >= total_tiles) return false;
+    w.t = s.next_tile;
+    w.kb0 = 0;
+    w.kb1 = 0;
+    w.slice = 0;
+    w.slices = 0;
+    s.next_tile += num_units;
+    ++s.i;
+    return true;
+}
+
+// k-blocks [begin, end) of a work item on problem pr
+__device__ __forceinline__ int work_kb_end(const Work& w, const Problem& pr) {
+    return (w.kb1 > 0 || w.slices > 0) ? w.kb1 : pr.k_blocks;
 }
 
 // ----------------------------------------------------------------------------------------
@@ -327,6 +457,7 @@ __device__ __forceinline__ TileCoord coord_of(const Params& p, const Work& w, in
 
 __device__ __forceinline__ void report_timeout(const Params& p, uint32_t role, int64_t tile, uint32_t stage,
                                                uint64_t waited) {
+    if (role == ROLE_DRAIN) atomicAdd(&p.err->drains, 1u);
     if (atomicCAS(&p.err->code, ERR_NONE, ERR_TIMEOUT) == ERR_NONE) {
         p.err->role = role;
         p.err->block = blockIdx.x;
@@ -394,11 +525,6 @@ __device__ __forceinline__ bool wait_quiet(uint32_t bar, uint32_t parity, uint64
     return true;
 }
 
-__device__ __forceinline__ void sleep_ns(uint64_t ns) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (ptx::globaltimer_ns() - t0 < ns) __nanosleep(1000);
-}
-
 // ----------------------------------------------------------------------------------------
 // epilogue math
 
@@ -424,6 +550,78 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 // ----------------------------------------------------------------------------------------
+// shared-memory words (own CTA)
+
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cta.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ----------------------------------------------------------------------------------------
+// after an abort: wait until the TMA loads this CTA (pair) issued have landed
+//
+// Positions are k-blocks counted along the unit's work items, the same sequence
+// in both CTAs of a pair; position x uses stage x % STAGES in phase (x / STAGES) & 1.
+// Only the last STAGES positions can still have loads in flight: a producer
+// loads position x only after the MMA released position x - STAGES, which
+// needed all of its bytes.  Every load signals the full barrier of the pair's
+// leader; the leader expects the bytes of both CTAs when it arrives.  So in a
+// pair, a position that only one CTA loaded (the other withheld it or had not
+// got there) is closed by the leader: complete_tx for the bytes that will never
+// come, or its own arrival with the other CTA's bytes.  Then each such phase
+// completes exactly when the issued bytes have landed, and the leader waits for
+// it; the other CTA stays in the cluster barrier of the teardown until then.
+template <class Cfg>
+__device__ __noinline__ void drain_issued_loads(const Params& p, uint32_t base) {
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int CG = Cfg::CTA_GROUP;
+    const uint32_t bar0 = base + Cfg::OFF_BAR;
+    const uint32_t pos0 = ld_shared_u32(base + Cfg::OFF_DRAIN_POS);
+    uint32_t pos1 = 0;
+    uint32_t last1[STAGES], bytes1[STAGES];
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) last1[s] = bytes1[s] = 0xffffffffu;
+    if constexpr (CG == 2) {
+        // the other CTA's ring record, once it is final
+        const uint32_t flag1 = ptx::mapa(base + Cfg::OFF_DRAIN_FLAG, 1);
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::ld_cluster_acquire_u32(flag1) == 0u) {
+            if (ptx::globaltimer_ns() - t0 > p.wait_budget_ns) {
+                report_timeout(p, ROLE_DRAIN, -1, 0, p.wait_budget_ns);
+                return;
+            }
+        }
+        pos1 = ptx::ld_cluster_u32(ptx::mapa(base + Cfg::OFF_DRAIN_POS, 1));
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            last1[s] = ptx::ld_cluster_u32(ptx::mapa(base + Cfg::OFF_DRAIN_LAST + 4 * s, 1));
+            bytes1[s] = ptx::ld_cluster_u32(ptx::mapa(base + Cfg::OFF_DRAIN_BYTES + 4 * s, 1));
+        }
+    }
+    const uint32_t top = pos0 > pos1 ? pos0 : pos1;
+    bool ok = true;
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+        if (top < static_cast<uint32_t>(s) + 1u) continue;             // stage never reached
+        const uint32_t x = top - 1u - ((top - 1u - s) % STAGES);        // its position in [top - STAGES, top)
+        const uint32_t bar = bar0 + 8u * s;
+        const bool a0 = ld_shared_u32(base + Cfg::OFF_DRAIN_LAST + 4 * s) == x;
+        const bool a1 = CG == 2 && last1[s] == x;
+        if constexpr (CG == 2) {
+            if (a0 && !a1) ptx::mbar_complete_tx(bar, ld_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * s));
+            else if (!a0 && a1) ptx::mbar_arrive_expect_tx(bar, bytes1[s]);
+        }
+        if (a0 || a1) ok = wait_quiet(bar, (x / STAGES) & 1u, p.wait_budget_ns) && ok;
+    }
+    if (!ok) report_timeout(p, ROLE_DRAIN, -1, 0, p.wait_budget_ns);
+}
+
+// ----------------------------------------------------------------------------------------
 // the kernel
 
 template <class Cfg>
@@ -431,6 +629,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     constexpr int STAGES = Cfg::STAGES;
     constexpr int CG = Cfg::CTA_GROUP;
     constexpr int BN = Cfg::BN;
+
+    const uint64_t t_entry = p.trace_ctas != nullptr ? ptx::globaltimer_ns() : 0;
 
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms (same offset in every CTA).
@@ -457,7 +657,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     const int64_t unit = blockIdx.x / CG;
     const int64_t num_units = gridDim.x / CG;
 
-    // ---- set-up: barriers, tensor memory
+    // ---- set-up: barriers, ring record, tensor memory
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
@@ -468,7 +668,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             ptx::mbar_init(tempty_bar(b), NUM_EPI_WARPS * CG);
         }
         ptx::mbar_init(drain_bar, 1);
-        asm volatile("st.shared::cta.u32 [%0], 0;" :: "r"(abort_addr) : "memory");
+        st_shared_u32(abort_addr, 0u);
+        st_shared_u32(base + Cfg::OFF_DRAIN_FLAG, 0u);
+        st_shared_u32(base + Cfg::OFF_DRAIN_POS, 0u);
+        for (int s = 0; s < MAX_STAGES; ++s) {
+            st_shared_u32(base + Cfg::OFF_DRAIN_LAST + 4 * s, 0xffffffffu);
+            st_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * s, 0u);
+        }
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -485,8 +691,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             long long rows = 0, tiles = 0;
             bool bad = false;
             if (lane == 0) { tile_pref[0] = 0; row_off[0] = 0; }
-            for (int base = 0; base < G; base += 32) {
-                const int i = base + lane;
+            for (int base_g = 0; base_g < G; base_g += 32) {
+                const int i = base_g + lane;
                 long long c = (i < G) ? static_cast<long long>(__ldg(p.moe_counts + i)) : 0ll;
                 bad |= c < 0;
                 c = c < 0 ? 0 : c;
@@ -527,27 +733,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + Cfg::OFF_TMEM_SLOT);
-    int64_t total_units = p.total_units;
+    int64_t total_tiles = p.total_tiles;
     MoeTable mt{};
     if constexpr (Cfg::MOE) {
-        total_units = *reinterpret_cast<volatile int32_t*>(smem + Cfg::OFF_MOE_TOTAL);
+        total_tiles = *reinterpret_cast<volatile int32_t*>(smem + Cfg::OFF_MOE_TOTAL);
         mt.tile_pref = reinterpret_cast<const int32_t*>(smem + Cfg::OFF_MOE);
         mt.row_off = mt.tile_pref + (MOE_MAX_G + 1);
     }
-    if (p.trace_ctas && threadIdx.x == 0 && blockIdx.x < p.trace_ctas_cap)
-        p.trace_ctas[2 * blockIdx.x] = ptx::globaltimer_ns();
+    if (p.trace_ctas && threadIdx.x == 0 && blockIdx.x < p.trace_ctas_cap) {
+        p.trace_ctas[4 * blockIdx.x + 0] = t_entry;
+        p.trace_ctas[4 * blockIdx.x + 1] = ptx::globaltimer_ns();
+    }
 
     if (warp == 0) {
         // ================================ TMA producer ================================
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            uint32_t pos = 0;            // ring positions advanced (k-blocks loaded or withheld)
             int g = 0, g_fenced = -1;
-            int64_t issued = 0;          // k-blocks whose loads this thread issued
             bool aborted = false;
-            bool withhold = (p.withhold_kb >= 0) && blockIdx.x == 0;
-            for (int64_t u = unit; u < total_units && !aborted; u += num_units) {
-                const Work w = work_of<Cfg>(p, u);
+            bool maps_ready = !Cfg::MOE;   // MoE: the per-expert maps come from the kernel before this one
+            bool withhold = (p.withhold_kb >= 0) && blockIdx.x == static_cast<uint32_t>(p.withhold_block);
+            // bytes each CTA loads per k-block; the leader's full barrier expects both CTAs'
+            constexpr uint32_t cta_tx = Cfg::A_BYTES + Cfg::B_BYTES;
+            Sched sc = sched_begin<Cfg>(p, unit);
+            Work w;
+            while (!aborted && sched_next<Cfg>(p, unit, num_units, total_tiles, sc, w)) {
                 g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 if constexpr (Cfg::GROUPED) {
@@ -557,22 +769,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         g_fenced = g;
                     }
                 }
-                const TileCoord tc = coord_of<Cfg>(p, w, g, rank, mt);
-                // first B column this CTA loads (an N-split unit uses the first half of each CTA's box)
-                const int nb0 = tc.n0 + static_cast<int>(rank) * (tc.nhalf ? Cfg::BN_CTA / 2 : Cfg::BN_CTA);
-                const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
-                // N-split units with N-contiguous B load only the 64-column boxes they use
-                const int b_boxes = (Cfg::B_MN && tc.nhalf) ? Cfg::BN_CTA / 128 : Cfg::BN_CTA / 64;
-                const uint32_t stage_tx = (Cfg::A_BYTES + (Cfg::B_MN ? b_boxes * 8192 : Cfg::B_BYTES)) * CG;
+                const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
+                const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // first B column this CTA loads
+                const int kb_end = work_kb_end(w, pr);
+                // A rows: the problem's map at row m0, or (MoE) the expert's own map at its local row
+                const CUtensorMap* map_a = &pr.tma_a;
+                int a_row = tc.m0;
+                if constexpr (Cfg::MOE) {
+                    map_a = p.moe_maps + 2 * g;
+                    a_row = tc.m0 - mt.row_off[g];
+                    if (!maps_ready) {
+                        ptx::grid_dependency_wait();
+                        maps_ready = true;
+                    }
+                    if (g != g_fenced) {
+                        ptx::fence_tensormap_acquire(map_a);
+                        g_fenced = g;
+                    }
+                }
                 for (int kb = w.kb0; kb < kb_end; ++kb) {
-                    if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, u, stage)) {
+                    if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, w.slot, stage)) {
                         aborted = true;
                         break;
                     }
                     const bool skip = withhold && kb == p.withhold_kb;
                     if (!skip) {
                         const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
-                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_tx);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), cta_tx * CG);
                         const int k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * Cfg::A_BYTES;
                         const uint32_t b_dst = sB + stage * Cfg::B_BYTES;
@@ -581,10 +804,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             else ptx::tma_load_2d(dst, m, x, y, fb);
                         };
                         if constexpr (Cfg::A_MN) {
-                            load(a_dst, &pr.tma_a, tc.m0, k0);
-                            load(a_dst + 8192, &pr.tma_a, tc.m0 + 64, k0);
+                            load(a_dst, map_a, a_row, k0);
+                            load(a_dst + 8192, map_a, a_row + 64, k0);
                         } else {
-                            load(a_dst, &pr.tma_a, k0, tc.m0);
+                            load(a_dst, map_a, k0, a_row);
                         }
                         if constexpr (Cfg::MOE) {
                             auto load3 = [&](uint32_t dst, int x, int y) {
@@ -593,20 +816,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             };
                             if constexpr (Cfg::B_MN) {
 #pragma unroll
-                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
-                                    if (j < b_boxes) load3(b_dst + j * 8192, nb0 + j * 64, k0);
+                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load3(b_dst + j * 8192, nb0 + j * 64, k0);
                             } else {
                                 load3(b_dst, k0, nb0);
                             }
                         } else if constexpr (Cfg::B_MN) {
 #pragma unroll
-                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
-                                if (j < b_boxes) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
                         } else {
                             load(b_dst, &pr.tma_b, k0, nb0);
                         }
-                        ++issued;
+                        st_shared_u32(base + Cfg::OFF_DRAIN_LAST + 4 * stage, pos);
+                        st_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * stage, cta_tx);
                     }
+                    ++pos;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 withhold = false;
@@ -622,11 +845,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            if (aborted && issued > 0) {
-                // Loads already issued still land in this CTA's shared memory:
-                // give them time (they complete without any consumer).
-                sleep_ns(200000);
-            }
+            // the ring record is final (the pair's leader reads the other CTA's after an abort)
+            st_shared_u32(base + Cfg::OFF_DRAIN_POS, pos);
+            ptx::st_release_cluster_u32(base + Cfg::OFF_DRAIN_FLAG, 1u);
+            if (aborted && leader) drain_issued_loads<Cfg>(p, base);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
@@ -650,34 +872,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 if (lane == 0) ok = wait_bounded<CG, false>(bar, par, p, abort_addr, ROLE_MMA, tile, st) ? 1u : 0u;
                 return __shfl_sync(0xffffffffu, ok, 0) != 0;
             };
-            for (int64_t u = unit; u < total_units && !aborted; u += num_units) {
-                const Work w = work_of<Cfg>(p, u);
+            Sched sc = sched_begin<Cfg>(p, unit);
+            Work w;
+            while (!aborted && sched_next<Cfg>(p, unit, num_units, total_tiles, sc, w)) {
                 g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
-                // half tiles: M = 128 for the pair (bits 24-28 of the instruction descriptor hold M >> 4);
-                // N-split units: N = BN/2 (bits 17-22 hold N >> 3)
-                const TileCoord tcm = coord_of<Cfg>(p, w, g, rank, mt);
+                // half tiles: M = 128 for the pair (bits 24-28 of the instruction descriptor hold M >> 4)
+                const TileCoord tcm = tile_coord<Cfg>(p, w.t, g, rank, mt);
                 uint32_t idesc = pr.idesc;
                 if (tcm.half) idesc = (idesc & ~(0x1Fu << 24)) | ((128u >> 4) << 24);
-                if (tcm.nhalf) idesc = (idesc & ~(0x3Fu << 17)) | ((static_cast<uint32_t>(BN / 2) >> 3) << 17);
-                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, u, 16 + acc)) {
+                if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, w.slot, 16 + acc)) {
                     aborted = true;
                     break;
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 const int kb_begin = w.kb0;
-                const int kb_end = w.tail >= 0 ? w.kb1 : pr.k_blocks;
-                const bool trace_unit = p.trace_tiles != nullptr && u < p.trace_tiles_cap;
+                const int kb_end = work_kb_end(w, pr);
+                const bool trace_unit = p.trace_tiles != nullptr && w.slot < p.trace_tiles_cap;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!warp_wait(full_bar(stage), phase, u, stage)) {
+                    if (!warp_wait(full_bar(stage), phase, w.slot, stage)) {
                         aborted = true;
                         break;
                     }
                     ptx::tc_fence_after_sync();
                     if (lane == 0 && kb == kb_begin && trace_unit) {
-                        p.trace_tiles[4 * u + 0] = blockIdx.x;
-                        p.trace_tiles[4 * u + 1] = ptx::globaltimer_ns();
+                        p.trace_tiles[4 * w.slot + 0] = blockIdx.x;
+                        p.trace_tiles[4 * w.slot + 1] = ptx::globaltimer_ns();
                     }
                     // stage s starts s * BYTES further on: add (s * BYTES) >> 4 to the start-address field
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * Cfg::A_BYTES) >> 4);
@@ -730,17 +951,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         uint32_t acc_phase = 0;
         int sbuf = 0;
         int g = 0, g_fenced = -1;
-        for (int64_t u = unit; u < total_units; u += num_units) {
-            const Work w = work_of<Cfg>(p, u);
+        bool maps_ready = !Cfg::MOE;
+        Sched sc = sched_begin<Cfg>(p, unit);
+        Work w;
+        while (sched_next<Cfg>(p, unit, num_units, total_tiles, sc, w)) {
             g = find_problem<Cfg>(p, w.t, g, mt);
             const Problem& pr = problem_of<Cfg>(p, g);
-            if constexpr (Cfg::GROUPED) {
+            // C: the problem's map, or (MoE) the expert's own map, whose rows end where its tokens do
+            const CUtensorMap* map_c = Cfg::MOE ? p.moe_maps + 2 * g + 1 : &pr.tma_c;
+            const int c_row_base = Cfg::MOE ? mt.row_off[g] : 0;
+            if constexpr (Cfg::GROUPED || Cfg::MOE) {
                 if (lane == 0 && g != g_fenced) {
-                    ptx::fence_tensormap_acquire(&pr.tma_c);
+                    if (!maps_ready) {
+                        ptx::grid_dependency_wait();
+                        maps_ready = true;
+                    }
+                    ptx::fence_tensormap_acquire(map_c);
                     g_fenced = g;
                 }
             }
-            const TileCoord tc = coord_of<Cfg>(p, w, g, rank, mt);
+            const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
             // half tiles: warps q and q + 2 share rows (q % 2) * 32 .. + 32 of this CTA's 64,
             // warp q / 2 == 1 taking columns [BN/2, BN)
             const int row0 = tc.m0 + (tc.half ? (q % 2) * 32 : q * 32);
@@ -748,10 +978,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             int row_limit = pr.M;                     // rows of C this tile may write: [.., row_limit)
             if constexpr (Cfg::MOE) row_limit = static_cast<int>(min(static_cast<int64_t>(tc.row_end), p.moe_rows));
             const bool active = row0 < row_limit;
-            // MoE: a slab that runs past its expert's rows is written row by row, without TMA
-            const bool direct = Cfg::MOE && row0 + 32 > row_limit;
             const int epi = pr.epi;
-            const bool has_acc = (w.tail >= 0 ? w.kb1 - w.kb0 : pr.k_blocks) > 0;
+            const bool has_acc = work_kb_end(w, pr) > w.kb0;
             const bool f16b = (pr.flags & FLAG_BIAS_F16) != 0;
 
             // The tile's bias, fetched before waiting for the accumulator so its latency
@@ -772,13 +1000,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             }
 
             uint32_t ok = 1;
-            if (lane == 0) ok = wait_bounded<CG>(tfull_bar(acc), acc_phase, p, abort_addr, ROLE_EPILOGUE, u, 16 + acc) ? 1u : 0u;
+            if (lane == 0) ok = wait_bounded<CG>(tfull_bar(acc), acc_phase, p, abort_addr, ROLE_EPILOGUE, w.slot, 16 + acc) ? 1u : 0u;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ptx::tc_fence_after_sync();
             __syncwarp();
-            const bool tracer = p.trace_tiles && lane == 0 && ew == 0 && leader && u < p.trace_tiles_cap;
-            if (tracer) p.trace_tiles[4 * u + 2] = ptx::globaltimer_ns();
+            const bool tracer = p.trace_tiles && lane == 0 && ew == 0 && leader && w.slot < p.trace_tiles_cap;
+            if (tracer) p.trace_tiles[4 * w.slot + 2] = ptx::globaltimer_ns();
 
             // RMS normalisation of A's row: one factor per accumulator row (this lane's row)
             float rs = 1.0f;
@@ -789,7 +1017,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             constexpr int CHUNKS = BN / Cfg::CW;
-            const int n_chunks = (tc.half || tc.nhalf) ? CHUNKS / 2 : CHUNKS;
+            const int n_chunks = tc.half ? CHUNKS / 2 : CHUNKS;
 
             // accumulator columns [c * CW, (c + 1) * CW) of this lane's row; the last chunk
             // hands the TMEM buffer back to the MMA issuer
@@ -858,19 +1086,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
                 // stage: this lane's row (128 bytes) as eight 16-byte chunks, 128-byte swizzled
                 const uint32_t buf = c_stage0 + sbuf * C_STAGE_BYTES;
-                if (!direct) {
-                    if (lane == 0) ptx::bulk_wait_group_read<1>();
-                    __syncwarp();
-                }
+                if (lane == 0) ptx::bulk_wait_group_read<1>();
+                __syncwarp();
                 const uint32_t row_addr = buf + lane * 128;
                 const bool c_f16 = (pr.flags & FLAG_C_F16) != 0;
-                constexpr int ESIZE = Cfg::C_F32 ? 4 : 2;
-                uint8_t* row_ptr = nullptr;           // direct stores: this lane's row of C
-                if constexpr (Cfg::MOE) {
-                    if (direct && row0 + lane < row_limit)
-                        row_ptr = static_cast<uint8_t*>(p.moe_c) +
-                                  (static_cast<int64_t>(row0 + lane) * p.moe_ldc + n_chunk) * ESIZE;
-                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint32_t w0, w1, w2, w3;
@@ -890,17 +1109,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         w2 = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
                         w3 = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
                     }
-                    if (direct) {
-                        // 16 bytes = 16 / ESIZE columns; N is a multiple of 8 on this path
-                        if (row_ptr && n_chunk + (j + 1) * (16 / ESIZE) <= pr.N)
-                            *reinterpret_cast<uint4*>(row_ptr + 16 * j) = make_uint4(w0, w1, w2, w3);
-                        continue;
-                    }
                     const uint32_t dst = row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
                                  :: "r"(dst), "r"(w0), "r"(w1), "r"(w2), "r"(w3) : "memory");
                 }
-                if (direct) return;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -910,16 +1122,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         const int j1 = static_cast<int>(static_cast<int64_t>(tc.r + 1) * pr.repeat / pr.replicas);
                         for (int j = j0; j < j1; ++j) ptx::tma_store_3d(&pr.tma_c, buf, n_chunk, j, row0);
                     } else {
-                        ptx::tma_store_2d(&pr.tma_c, buf, n_chunk, row0);
+                        ptx::tma_store_2d(map_c, buf, n_chunk, row0 - c_row_base);
                     }
                     ptx::bulk_commit_group();
                 }
                 sbuf ^= 1;
             };
 
-            bool whole = true;
-            if constexpr (!Cfg::GROUPED && !Cfg::MOE) whole = w.tail < 0;
-            if (whole) {
+            if (w.slices == 0) {
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     float v[Cfg::CW];
@@ -927,16 +1137,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     finish_chunk(c, v);
                 }
             } else {
-                // Slice of a split tile: this warp's 32 x BN partial sums go to its own slab,
-                // float4 [column / 4][lane] so a warp's stores are 512 contiguous bytes.
-                const int S = p.sk_slices;
+                // Stream-K piece: this warp's 32 x BN partial sums go to its own slab,
+                // float4 [column / 4][lane] so that a warp's stores are 512 contiguous bytes.
+                const int S = w.slices;
                 constexpr int64_t SLAB = 32 * BN;
                 auto slab = [&](int slice) {
                     return reinterpret_cast<float4*>(
-                        p.sk_partial + ((static_cast<int64_t>(w.tail) * S + slice) * CG + rank) * 4 * SLAB + q * SLAB);
+                        p.sk_partial + (((w.t * p.sk_max_slices + slice) * CG + rank) * 4 + q) * SLAB);
                 };
                 float4* mine = slab(w.slice);
-                // the accumulator stays in TMEM until it is known whether this slice adds up
+                // the accumulator stays in TMEM until it is known whether this piece adds up
 #pragma unroll 1
                 for (int c = 0; c < CHUNKS; ++c) {
                     float v[Cfg::CW];
@@ -955,21 +1165,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     __syncwarp();
                     if (lane == 0) {
                         ptx::grid_dependency_wait();   // the counters were zeroed by the kernel before this one
-                        const uint32_t idx = (static_cast<uint32_t>(w.tail) * CG + rank) * 4 + q;
+                        const uint32_t idx = (static_cast<uint32_t>(w.t) * CG + rank) * 4 + q;
                         last = atomicAdd(p.sk_count + idx, 1u) == static_cast<uint32_t>(S - 1) ? 1u : 0u;
                     }
                     last = __shfl_sync(0xffffffffu, last, 0);
                 }
-                if (last) {
-                    // The other slices' partials are visible.  Add all S in slice order, this
-                    // slice's own from TMEM (the same values it stored).  The others stream
-                    // through this warp's share of the operand ring - idle now, because a
-                    // slice is always its CTA's last work unit - with cp.async, FIX_BUFS
-                    // chunks in flight; each lane copies and reads back only its own float4s.
+                // the unit's last work item: its operand ring is idle from here on
+                Sched peek = sc;
+                Work after;
+                const bool unit_done = !sched_next<Cfg>(p, unit, num_units, total_tiles, peek, after);
+                if (last && unit_done) {
+                    // Every piece's partials are visible.  Add all S in k order, this piece's own
+                    // from TMEM (the same values it stored).  The others stream through this warp's
+                    // share of the operand ring - idle, as no MMA or load of this unit is left - with
+                    // cp.async, FIX_BUFS chunks in flight; each lane copies and reads back only its
+                    // own float4s.
                     __threadfence();
                     constexpr int CH_BYTES = 32 * Cfg::CW * 4;
                     const uint32_t region = sA + static_cast<uint32_t>(q) * FIX_BUFS * CH_BYTES;
-                    const int items = CHUNKS * (S - 1);      // (chunk, other slice), chunk-major
+                    const int items = CHUNKS * (S - 1);      // (chunk, other piece), chunk-major
                     auto issue = [&](int k) {
                         if (k < items) {
                             const int c = k / (S - 1), j = k % (S - 1);
@@ -1016,8 +1230,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         finish_chunk(c, v);
                     }
                     ptx::cp_async_wait<0>();
+                } else if (last) {
+                    // Every piece's partials are visible.  Add all S in k order, this piece's own
+                    // from TMEM (the same values it stored), the others from L2; the operand ring
+                    // belongs to the unit's next work item, so they come straight into registers.
+                    __threadfence();
+#pragma unroll 1
+                    for (int c = 0; c < CHUNKS; ++c) {
+                        float v[Cfg::CW];
+#pragma unroll 1
+                        for (int sl = 0; sl < S; ++sl) {
+                            float x[Cfg::CW];
+                            if (sl == w.slice) {
+                                read_chunk(c, x, c == CHUNKS - 1);
+                            } else {
+                                const float4* src = slab(sl) + c * (Cfg::CW / 4) * 32 + lane;
+#pragma unroll
+                                for (int i = 0; i < Cfg::CW / 4; ++i) {
+                                    const float4 y = __ldcg(src + i * 32);
+                                    x[4 * i] = y.x;
+                                    x[4 * i + 1] = y.y;
+                                    x[4 * i + 2] = y.z;
+                                    x[4 * i + 3] = y.w;
+                                }
+                            }
+                            if (sl == 0) {
+#pragma unroll
+                                for (int i = 0; i < Cfg::CW; ++i) v[i] = x[i];
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < Cfg::CW; ++i) v[i] += x[i];
+                            }
+                        }
+                        finish_chunk(c, v);
+                    }
                 } else {
-                    // not the last slice (or no rows here): hand the accumulator back
+                    // not the last piece (or no rows here): hand the accumulator back
                     ptx::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
@@ -1026,7 +1274,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     }
                 }
             }
-            if (tracer) p.trace_tiles[4 * u + 3] = ptx::globaltimer_ns();
+            if (tracer) p.trace_tiles[4 * w.slot + 3] = ptx::globaltimer_ns();
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();
@@ -1036,11 +1284,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     // ---- teardown (lanes 1-31 of warps 0 and 1 wait here for their lane 0)
     __syncwarp();
     if (p.trace_ctas && warp == EPI_WARP0 && lane == 0 && blockIdx.x < p.trace_ctas_cap)
-        p.trace_ctas[2 * blockIdx.x + 1] = ptx::globaltimer_ns();
+        p.trace_ctas[4 * blockIdx.x + 2] = ptx::globaltimer_ns();
     ptx::tc_fence_before_sync();
     if constexpr (CG == 2) ptx::cluster_sync(); else __syncthreads();
     ptx::tc_fence_after_sync();
     if (warp == 1) ptx::tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
+    if (p.trace_ctas && warp == 1 && lane == 0 && blockIdx.x < p.trace_ctas_cap)
+        p.trace_ctas[4 * blockIdx.x + 3] = ptx::globaltimer_ns();
 }
 
 }  // namespace tg

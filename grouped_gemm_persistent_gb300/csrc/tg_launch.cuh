@@ -20,11 +20,16 @@ template <class Cfg>
 cudaError_t resident_units(int* units);
 
 // tg_aux.cu.  r[i] = 1 / sqrt(mean_k A[i][k]^2 + eps) for a row-major bf16 A; the
-// first block also zeroes counters[0, n_counters) (split tiles of the GEMM that follows).
+// first block also zeroes counters[0, n_counters) (stream-K tiles of the GEMM that follows).
 cudaError_t launch_row_rms(const void* A, int64_t lda, int64_t M, int64_t K, float eps, float* r, int sms,
                            cudaStream_t stream, uint32_t* counters = nullptr, int n_counters = 0);
 // counters[0, n) = 0, as a kernel the GEMM can follow as a programmatic dependent.
 cudaError_t launch_clear_counters(uint32_t* counters, int n, cudaStream_t stream);
+// maps[2 g], maps[2 g + 1] = expert g's A and C maps (templates over all T rows narrowed
+// to the expert's rows from the device counts), for the device-counts MoE GEMM.
+cudaError_t launch_moe_maps(const CUtensorMap& tmpl_a, const CUtensorMap& tmpl_c, const int32_t* counts, int G,
+                            const void* A, int64_t a_row_bytes, void* C, int64_t c_row_bytes, int64_t T,
+                            CUtensorMap* maps, cudaStream_t stream);
 
 }  // namespace tg
 

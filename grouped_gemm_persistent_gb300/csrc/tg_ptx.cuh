@@ -60,6 +60,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
 
+// Count `bytes` of the current phase's expected transactions as done without
+// any data arriving (used only to close a phase whose loads were never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
 // Like mbar_try_wait, but the thread may be suspended (not issuing) for up to
 // `suspend_ns` while the phase is incomplete; it wakes when the phase completes.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
@@ -84,6 +90,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ----------------------------------------------------------------------------------------
+// shared memory of the peer CTA (addresses from mapa)
+
+__device__ __forceinline__ uint32_t ld_cluster_acquire_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cluster.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Store to own shared memory, ordered after this thread's earlier shared-memory
+// stores for any CTA of the cluster that reads it with ld_cluster_acquire_u32.
+__device__ __forceinline__ void st_release_cluster_u32(uint32_t smem_addr, uint32_t v) {
+    asm volatile("st.release.cluster.shared::cta.u32 [%0], %1;" :: "r"(smem_addr), "r"(v) : "memory");
+}
+
+// ----------------------------------------------------------------------------------------
 // proxy fences
 
 // Generic-proxy writes to shared memory -> visible to the async proxy (TMA store source).
@@ -95,6 +122,24 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // the tensormap proxy before its first use by this thread.
 __device__ __forceinline__ void fence_tensormap_acquire(const void* tmap) {
     asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;" :: "l"(tmap) : "memory");
+}
+
+// Tensor-map fields rewritten in global memory (tile mode): the base address, and
+// the extent of dimension `dim` (elements).
+__device__ __forceinline__ void tensormap_replace_address(void* tmap, const void* addr) {
+    asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;"
+                 :: "l"(tmap), "l"(reinterpret_cast<uint64_t>(addr)) : "memory");
+}
+
+template <int DIM>
+__device__ __forceinline__ void tensormap_replace_dim(void* tmap, uint32_t extent) {
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], %1, %2;"
+                 :: "l"(tmap), "n"(DIM), "r"(extent) : "memory");
+}
+
+// Tensor maps this thread wrote become visible to the tensormap proxy of the GPU.
+__device__ __forceinline__ void fence_tensormap_release() {
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {

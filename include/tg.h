@@ -37,16 +37,16 @@
  *  - Degenerate sizes: M == 0 or N == 0 is a no-op returning TG_OK.  K == 0
  *    is the empty sum: C = epilogue(0), i.e. zeros, bias, or GELU(bias).
  *  - Results are deterministic: two identical calls write bitwise-identical C.
- *    Dense calls split the tiles of their last, partial wave: into two column
- *    halves when there is room (256-wide tiles; the arithmetic per element is
- *    unchanged), else into several K-ranges on different SMs whose fp32
- *    partials are added in a fixed order (an atomic counter only picks which
- *    SM does the adding), so the result does not depend on timing.  Set
- *    TG_SPLIT_TAIL=0 in the environment to turn splitting off (one K-order per
- *    tile, as grouped calls), TG_SPLIT_TAIL=k to always cut along K.
- *  - Dense calls with K-range splits take a workspace from a library-owned
- *    stream-ordered memory pool (at most (resident CTAs) x 128 KiB, released
- *    on the stream after the launch).
+ *    A dense call whose tiles do not divide evenly over the SMs runs stream-K:
+ *    the k-blocks of the tiles of its last, partial wave are cut into equal
+ *    ranges, one per CTA (pair), which run first; the fp32 partial sums of a
+ *    tile's pieces are added in k order (an atomic counter only picks which SM
+ *    does the adding), so the result does not depend on timing.  Set
+ *    TG_STREAM_K=0 in the environment to turn it off (one K order per tile, as
+ *    grouped calls).
+ *  - Dense stream-K calls take a workspace from a library-owned stream-ordered
+ *    memory pool (up to 9 x 256 KiB per stream-K tile, fewer than the resident
+ *    CTA pairs; released on the stream after the launch).
  */
 #ifndef TG_H
 #define TG_H
@@ -101,6 +101,14 @@ typedef enum {
  * Accumulation is fp32 in tensor memory; the epilogue runs in fp32 and rounds
  * once.  Each element agrees with the exact result within
  * 1e-2 * sum_k |a_ik b_kj| (+ 1e-2 |bias_j|) + 1e-5.
+ *
+ * Source: "How We Built TLX", section "Introducing TLX": the standard Triton
+ * matmul listing (an fp32 accumulator summed over BLOCK_K steps of A and B
+ * tiles) and the TLX-on-Blackwell listing (TMA loads into a barrier-guarded
+ * ring, MMAs into a tensor-memory accumulator, a separate epilogue); and the
+ * tile tutorial "Guide de programmation pour la programmation GPU par tuiles
+ * de NVIDIA", its fused kernel that multiplies, adds a bias and applies GELU
+ * in one pass.
  */
 tg_status tg_gemm(const void *A, tg_layout layout_a, int64_t lda,
                   const void *B, tg_layout layout_b, int64_t ldb,
@@ -120,8 +128,8 @@ tg_status tg_gemm(const void *A, tg_layout layout_a, int64_t lda,
  * broadcasts inside the kernel.  Each distinct result row is computed once per
  * replica CTA and stored `repeat` times, so A costs U*K*2 bytes of traffic
  * instead of U*repeat*K*2.  Results are bitwise identical to tg_gemm on the
- * materialised A when that call does not split its last wave along K (always
- * with TG_SPLIT_TAIL=0), and within the stated tolerance otherwise.
+ * materialised A when that call runs without stream-K (always with
+ * TG_STREAM_K=0), and within the stated tolerance otherwise.
  *
  *   A_user, layout_a, lda : bf16 U x K (row-major: lda >= K; column-major: lda >= U).
  *   repeat                : >= 1; U * repeat < 2^31.
@@ -138,15 +146,24 @@ tg_status tg_gemm_bcast(const void *A_user, tg_layout layout_a, int64_t lda, int
  * tg_row_rms - r[i] = 1 / sqrt((1/K) sum_k A[i][k]^2 + eps) for a row-major bf16
  * A [M, K] (lda >= K, 16-byte aligned rows); r is a DEVICE fp32 [M].  Sums run
  * in fp32 in a fixed order (deterministic).  K == 0 gives r = 1 / sqrt(eps).
+ * The row statistics of the normalisation that tg_gemm_rmsnorm fuses into the
+ * GEMM (same source as tg_gemm_rmsnorm).
  */
 tg_status tg_row_rms(const void *A, int64_t lda, int64_t M, int64_t K, float eps, float *r, tg_stream_t stream);
 
 /*
  * tg_gemm_rmsnorm - C = epilogue(rmsnorm(A) . B), the normalisation fused
- * into the GEMM (the TLX pages' "fuse the norm into the GEMM" idea): since
- * rmsnorm(A) = diag(r) A, the product is computed on A as stored and row i of
- * the fp32 accumulator is scaled by r_i in the epilogue, before bias and GELU;
- * the normalised A is never written or read back.  r comes from tg_row_rms
+ * into the GEMM.  Source: the Chinese rewrite of "How We Built TLX" ("Meta 造了
+ * 个 Triton 扩展 TLX ..."), section on what TLX provides: because layouts are
+ * inferred, a normalisation can be fused into the GEMM and the intermediate
+ * round trip through memory disappears; and the companion article it lists,
+ * "Achieving Free Normalization: Fusing Norms into GEMM and Attention via TLX"
+ * (title only; the pages give no formula, RMS normalisation is this library's
+ * reading).
+ *
+ * Since rmsnorm(A) = diag(r) A, the product is computed on A as stored and
+ * row i of the fp32 accumulator is scaled by r_i in the epilogue, before bias
+ * and GELU; the normalised A is never written or read back.  r comes from tg_row_rms
  * (one read of A) and is left in row_scale (DEVICE fp32 [M]) for reuse.  A
  * gain vector gamma folds into B: rmsnorm_gamma(A) . B = rmsnorm(A) . diag(gamma) B.
  * A is row-major bf16; other arguments as tg_gemm.  With K == 0 the result is
@@ -176,13 +193,22 @@ typedef struct tg_group_problem {
  * tg_gemm_ex - one dense GEMM described by a problem record (fields as for
  * tg_gemm), which also selects fp16 operands (ab_dtype = TG_F16, the element
  * type of the TLX listing) and an fp16 output (c_dtype = TG_F16).  The record
- * is read during the call only.
+ * is read during the call only.  Source: as tg_gemm; the fp16 element type is
+ * the one the TLX-on-Blackwell listing ("How We Built TLX", section
+ * "Introducing TLX") declares for its operands and output.
  */
 tg_status tg_gemm_ex(const tg_group_problem *problem, tg_stream_t stream);
 
 /*
  * tg_grouped_gemm - G independent GEMMs in one persistent launch (one launch
  * per distinct (layout_a, layout_b, c_dtype) combination present).
+ *
+ * Source: "How We Built TLX", case-study table (LLM pre-training row) and
+ * "Case study 3: distributed grouped GEMM for LLM pre-training": the grouped
+ * matrix multiplies of a mixture-of-experts layer, one GEMM per expert with a
+ * ragged number of tokens (rows), run as one persistent kernel.  This call is
+ * one GPU's share of that kernel; the token exchange between GPUs is not part
+ * of it.
  *
  *   table : HOST array of G problems.  It is read during the call and may be
  *           reused or freed as soon as the call returns.
@@ -202,9 +228,16 @@ tg_status tg_grouped_gemm(const tg_group_problem *table, int G, tg_stream_t stre
 
 /*
  * tg_moe_gemm - MoE expert GEMM whose per-expert token counts are in DEVICE
- * memory, as a router running on the GPU produces them: one launch, no
- * host round trip and no per-expert descriptors (the MoE layer of the TLX
- * article's third case study, with counts that never leave the GPU).
+ * memory, as a router running on the GPU produces them: no host round trip
+ * (the MoE layer of the TLX article's third case study, "Distributed grouped
+ * GEMM for LLM pre-training", with counts that never leave the GPU).  A
+ * one-warp kernel reads the counts and writes each expert's own A and C tensor
+ * maps on the device (tensormap.replace on copies of maps over all T rows); the
+ * GEMM, launched as its programmatic dependent, schedules its tiles from the
+ * same counts and loads and stores through those maps, so a tile that runs
+ * past an expert's rows reads zeros and writes nothing beyond them.  The maps
+ * take 256 bytes per expert of a stream-ordered workspace from the library's
+ * memory pool, released on the stream after the launch.
  *
  *   A, lda, T, K     : bf16 [T, K] row-major; expert g owns rows
  *                      [off_g, off_g + counts[g]), off_g = counts[0] + ... + counts[g-1].
@@ -217,8 +250,8 @@ tg_status tg_grouped_gemm(const tg_group_problem *table, int G, tg_stream_t stre
  *                      of the counts are not written.
  *   epi, bias        : bias is bf16 [G, N] (row g for expert g).
  *
- * Limits: G <= TG_MOE_MAX_EXPERTS; N a multiple of 8; TMA alignment rules as
- * for tg_gemm; expert_stride a multiple of 8 elements.  Counts that are
+ * Limits: G <= TG_MOE_MAX_EXPERTS; TMA alignment rules as for tg_gemm;
+ * expert_stride a multiple of 8 elements.  Counts that are
  * negative or sum to more than T make the launch compute nothing and
  * tg_device_status report TG_ERR_INVALID_ARG.  Results are bitwise equal to
  * tg_grouped_gemm on the same rows.
@@ -258,19 +291,42 @@ tg_status tg_moe_gemm(const void *A, int64_t lda, int64_t T, int64_t K,
  */
 tg_status tg_grouped_gemm_noalloc(const tg_group_problem *table, int G, tg_stream_t stream);
 
-/* Static English description of a status code (never NULL). */
+/*
+ * tg_status_string - static English description of a status code (never NULL;
+ * an unknown code gives "unknown status").
+ *
+ * Source: "How We Built TLX", section "Lessons: advice for building a GPU
+ * compiler", point "The compiler is part of the user interface": error
+ * messages and debugging support weigh as much as the quality of the generated
+ * code, because the engineer chasing a utilisation or synchronisation problem
+ * needs plain feedback.  Every entry point therefore returns a status code
+ * with a fixed meaning, and tg_last_error_message adds the detail.
+ */
 const char *tg_status_string(tg_status status);
 
 /*
- * Description of the most recent failing call on the calling thread (argument
- * check, CUDA error or in-kernel timeout, with the offending value or problem
- * index).  Owned by the library, valid until the thread's next libtg call.
+ * tg_last_error_message - what the most recent failing call on the calling
+ * thread found (argument check, CUDA error or in-kernel timeout), naming the
+ * offending value or problem index.  Same source as tg_status_string.  The
+ * string is owned by the library and valid until the thread's next libtg
+ * call; it is empty if no call has failed yet.
  */
 const char *tg_last_error_message(void);
 
 /*
  * tg_device_status - synchronise `stream`, then read and clear the current
- * device's error record.  Returns TG_OK, TG_ERR_CUDA (the stream reported a
+ * device's error record.
+ *
+ * Source: "How We Built TLX", "Case study 3": at the scale of weeks-long
+ * pre-training runs, reliability and debuggability count as much as peak
+ * throughput; and the Chinese rewrite of the same article ("Meta 造了个 Triton
+ * 扩展 TLX ..."), editor's commentary, third point: a hung warp-specialised
+ * mega-kernel is hard to locate, so hang detection belongs in the test setup
+ * before such a kernel is adopted.  Here every in-kernel wait is bounded and
+ * its expiry is recorded on the device and reported by this call, which
+ * allocates nothing.
+ *
+ * Returns TG_OK, TG_ERR_CUDA (the stream reported a
  * CUDA error), TG_ERR_INVALID_ARG (tg_moe_gemm found invalid device counts),
  * or TG_ERR_TIMEOUT (a kernel's bounded mbarrier wait ran out:
  * the kernel recorded the role, tile and stage, stopped, drained its own
@@ -287,26 +343,31 @@ tg_status tg_device_status(tg_stream_t stream);
 tg_status tg_set_wait_budget_ms(uint32_t ms);
 
 /*
- * Test hook for the failure path.  The next launch made by this thread has
- * its TMA producer withhold the arrival for the k-block with global index
- * `k_block` of its first tile, so the MMA issuer's bounded wait on that stage
- * runs out and tg_device_status reports TG_ERR_TIMEOUT.  -1 (the default)
- * disables it; the hook disarms itself after one launch.  Nothing faults.
+ * Test hooks for the failure path.  The next launch made by this thread has
+ * the TMA producer of CTA `block` (blockIdx.x; 0 for tg_debug_withhold_stage)
+ * withhold the arrival and the loads for the k-block with index `k_block` of
+ * its first work item (a k-block of a tile, counted from the tile's first), so
+ * that a bounded wait on that stage runs out (in a CTA pair the MMA issuer of
+ * the pair's first CTA waits for both CTAs' loads) and tg_device_status
+ * reports TG_ERR_TIMEOUT.  -1 (the default) disables it; the hook disarms
+ * itself after one launch.  Nothing faults: after the timeout the kernel waits
+ * for the loads that were issued and returns.
  */
 tg_status tg_debug_withhold_stage(int64_t k_block);
+tg_status tg_debug_withhold_stage_in(int64_t k_block, int32_t block);
 
 /*
  * Timeline trace of the next launch made by this thread (a profiling aid; off
  * by default, disarms itself after one launch).  Both buffers are DEVICE
  * memory owned by the caller; the kernel writes, with %globaltimer nanosecond
  * stamps:
- *   tile_records[4 w .. 4 w + 3] for work unit w < tile_capacity:
+ *   tile_records[4 s .. 4 s + 3] for work slot s < tile_capacity:
  *       {block index, first k-block ready for the MMA, accumulator complete,
- *        epilogue done}.  A work unit is a tile, or one K-range of a split
- *       tile (dense calls split the tiles of their last, partial wave); CTA
- *       (pair) i runs units i, i + U, i + 2U, ... for U resident CTAs (pairs);
- *   cta_records[2 b .. 2 b + 1] for block b < cta_capacity:
- *       {set-up done, teardown start}.
+ *        epilogue done}.  A work item is a tile, or one stream-K piece (a
+ *       k-block range) of a tile; the i-th item of CTA (pair) u of U has slot
+ *       i * U + u, so a unit with fewer items leaves its later slots untouched;
+ *   cta_records[4 b .. 4 b + 3] for block b < cta_capacity:
+ *       {kernel entry, set-up done, teardown start, exit}.
  * Capacities may be 0 to skip a buffer.  Grouped calls with several layout
  * classes trace only their first launch.
  */
@@ -315,6 +376,14 @@ tg_status tg_debug_trace(uint64_t *tile_records, int64_t tile_capacity,
 
 /* Library version as (major << 16) | minor. */
 uint32_t tg_version(void);
+
+/*
+ * Number of CUDA kernels the calling thread has enqueued through libtg since
+ * the library was loaded (GEMM launches and the small kernels some calls run
+ * before them: the row statistics of tg_gemm_rmsnorm, the counter reset of a
+ * dense stream-K launch).  Benchmarks report the difference over a timed region.
+ */
+uint64_t tg_launch_count(void);
 
 #ifdef __cplusplus
 }

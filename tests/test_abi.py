@@ -52,7 +52,8 @@ def test_status_strings(lib):
         s = lib.tg_status_string(code)
         assert s and isinstance(s, bytes)
     assert lib.tg_status_string(99) == b"unknown status"
-    assert lib.tg_version() == (0 << 16) | 1
+    assert lib.tg_version() == (0 << 16) | 2
+    assert lib.tg_launch_count() == 0     # no kernel was enqueued by this thread
 
 
 def test_degenerate_sizes_are_noops(lib):
@@ -93,8 +94,20 @@ def test_bad_arguments(lib, kwargs, code):
     assert lib.tg_last_error_message()  # a description is always left behind
 
 
+def _no_gpu():
+    # Calls below pass the host checks with fake addresses; with a GPU present they
+    # would launch on them, so they only run where there is none.
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("the call would reach a real device with fake addresses")
+    except ImportError:
+        pass
+
+
 def test_k_zero_needs_no_operands(lib):
     # K == 0 passes the checks with NULL A/B and odd ld (then needs a device)
+    _no_gpu()
     rc = gemm(lib, A=NULL, B=NULL, lda=0, ldb=0, K=0)
     assert rc != tg.TG_ERR_INVALID_ARG and rc != tg.TG_ERR_UNSUPPORTED
 
@@ -173,9 +186,11 @@ def test_moe_argument_checks(lib):
     assert moe(G=191) == tg.TG_ERR_UNSUPPORTED                          # schedule table limit
     assert moe(counts=None) == tg.TG_ERR_INVALID_ARG
     assert moe(counts=0x40002) == tg.TG_ERR_INVALID_ARG                 # counts must be 4-byte aligned
-    assert moe(N=60) == tg.TG_ERR_UNSUPPORTED                           # N % 8
     assert moe(stride=64 * 63) == tg.TG_ERR_INVALID_ARG                 # one expert does not fit its stride
     assert moe(T=-1) == tg.TG_ERR_INVALID_ARG
+    _no_gpu()
+    rc = moe(N=60)                                                      # any N: per-expert maps clip the columns
+    assert rc not in (tg.TG_ERR_INVALID_ARG, tg.TG_ERR_UNSUPPORTED)
 
 
 def test_rmsnorm_argument_checks(lib):

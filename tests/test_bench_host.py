@@ -86,3 +86,13 @@ def test_reference_arm_stays_within_minutes():
         total = per * (steps + warmup / 4)
         assert 0.01 <= per <= 10.0
         assert total <= 70.0 or per == 0.01, (steps, warmup, total)
+
+
+def test_code_digest_ignores_comments_and_blank_lines():
+    # the traffic record is keyed by this digest: documentation edits must not change it
+    from grouped_gemm_persistent_gb300.build import _strip_comments, code_digest
+    src = 'int a = 1; // note\n/* block\n comment */ const char* s = "a//b /* c */";\n\n  char q = \'"\'; int b; /* t */\n'
+    assert _strip_comments(src) == 'int a = 1;\n const char* s = "a//b /* c */";\n  char q = \'"\'; int b;'
+    assert _strip_comments("x = 1;  // one\n") == _strip_comments("x = 1;\n\n/* two */\n")
+    assert _strip_comments("x = 1;") != _strip_comments("x = 2;")
+    assert code_digest() == code_digest() and len(code_digest()) == 64

@@ -270,7 +270,7 @@ def test_bcast_matches_materialised(U, repeat, N, K, epi):
 
 
 def test_bcast_equals_dense_on_materialised_bitwise(monkeypatch):
-    monkeypatch.setenv("TG_SPLIT_TAIL", "0")    # same summation order on both paths
+    monkeypatch.setenv("TG_STREAM_K", "0")    # same summation order on both paths
     case = wl.dense_case("skinny_bcast")
     dense = run_dense(case)
     bc = tg.gemm_bcast(case.users.cuda(), case.b.cuda(), case.repeat, bias=case.bias.cuda(), epilogue="bias")
@@ -330,7 +330,7 @@ def test_grouped_ragged_with_empty_groups(epi, b_col, tile):
 
 
 def test_grouped_single_group_matches_dense_bitwise(tile, monkeypatch):
-    monkeypatch.setenv("TG_SPLIT_TAIL", "0")    # same summation order on both paths
+    monkeypatch.setenv("TG_STREAM_K", "0")    # same summation order on both paths
     case = wl.dense_random(700, 392, 320, seed=22, dist="normal", epi="bias")
     a, b, bias = case.a.cuda(), case.b.cuda(), case.bias.cuda()
     dense = tg.gemm(a, b, bias=bias, epilogue="bias")
@@ -485,19 +485,31 @@ def test_workload_grouped_moe_device_counts_bitwise():
 
 # ------------------------------------------------------------------------------------------ failure path
 
-def test_bounded_wait_reports_timeout_and_context_survives(tile):
-    case = wl.dense_random(256, 256, 512, seed=30, dist="normal")
+# Block 0's first work item at 256 x 256 x 4096 is a stream-K range of k-blocks
+# [0, 8) in every variant; a single CTA's block 1 has [8, 16), a pair's block 1
+# shares block 0's.  Withholding k-block 3 or 5 leaves the later stages of the
+# ring loaded when the wait runs out; withholding in a pair's second CTA leaves
+# a phase that the first CTA loaded but its partner did not, which the abort
+# path closes before it waits for the loads that were issued.
+@pytest.mark.parametrize("block,kb", [(0, 3), (0, 5), (1, 5)])
+def test_bounded_wait_reports_timeout_and_context_survives(tile, block, kb):
+    case = wl.dense_random(256, 256, 4096, seed=30, dist="normal")
     a, b = case.a.cuda(), case.b.cuda()
+    if block == 1 and tile.startswith("1x"):
+        kb += 8
     tg.set_wait_budget_ms(100)
     try:
-        tg.debug_withhold_stage(3)           # the first CTA never gets k-block 3 of its first tile
+        tg.debug_withhold_stage(kb, block=block)
         tg.gemm(a, b)
         with pytest.raises(tg.TGError) as ei:
             tg.device_status()
         assert ei.value.status == tg.TG_ERR_TIMEOUT
         assert "role=" in str(ei.value)
+        assert "; 0 abort-path drains ran out" in str(ei.value), str(ei.value)
     finally:
         tg.set_wait_budget_ms(0)
+    # nothing else was recorded after the timeout (the drain of the issued loads finished in time)
+    tg.device_status()
     # the context is still usable and the record was cleared
     c = run_dense(case)
     _sync_ok()
@@ -510,7 +522,7 @@ def test_timeline_trace_records_every_tile(tile):
     case = wl.dense_random(1000, 1000, 512, seed=31, dist="normal")
     a, b = case.a.cuda(), case.b.cuda()
     tiles = torch.zeros((4096, 4), dtype=torch.int64, device="cuda")
-    ctas = torch.zeros((1024, 2), dtype=torch.int64, device="cuda")
+    ctas = torch.zeros((1024, 4), dtype=torch.int64, device="cuda")
     tg.debug_trace(tiles, ctas)
     c = tg.gemm(a, b)
     _sync_ok()
@@ -518,13 +530,22 @@ def test_timeline_trace_records_every_tile(tile):
     tr = tiles.cpu().numpy()
     used = tr[:, 1] > 0
     n = int(used.sum())
-    assert n > 0 and used[:n].all() and not used[n:].any(), "tiles are traced densely from index 0"
-    t = tr[:n]
+    assert n > 0 and not used[2048:].any()
+    t = tr[used]
     assert (t[:, 1] <= t[:, 2]).all() and (t[:, 2] <= t[:, 3]).all()
     cr = ctas.cpu().numpy()
     live = cr[:, 0] > 0
-    assert live.any() and (cr[live, 0] <= cr[live, 1]).all()
+    assert live.any()
+    # {entry, set-up done, teardown start, exit} in order for every block that ran
+    assert (cr[live, 0] <= cr[live, 1]).all() and (cr[live, 1] <= cr[live, 2]).all()
+    assert (cr[live, 2] <= cr[live, 3]).all()
     assert set(t[:, 0].tolist()) <= set(np.flatnonzero(live).tolist())
+    # slot i * U + u holds the i-th item of unit u: a unit's items run in slot order
+    U = int(live.sum()) // (2 if tile.startswith("2x") else 1)
+    for u in range(U):
+        mine = tr[u::U]
+        mine = mine[mine[:, 1] > 0]
+        assert (np.diff(mine[:, 1]) > 0).all(), "a unit's work items start in slot order"
     # the trace disarms itself: a second launch leaves a fresh buffer untouched
     tiles2 = torch.zeros_like(tiles)
     tg.gemm(a, b)
@@ -532,44 +553,48 @@ def test_timeline_trace_records_every_tile(tile):
     assert not tiles2.any()
 
 
-# ------------------------------------------------------------------------------------------ split tiles
-# The last, partial wave of a dense launch is split.  With 256-wide tiles and
-# room for twice its tiles, each tile becomes two column halves (N = 128 MMAs).
-# Otherwise each tile is cut along K and computed by several CTAs (pairs) at
-# once; the last to finish adds the fp32 partials in slice order
-# (TG_SPLIT_TAIL=k forces the K-cut).  Shapes below: (a) more tiles than
-# resident pairs, with a small remainder (2304^2: 81 pair tiles on 76 pairs);
-# (b) fewer tiles than CTAs (512^2 x 2048: 8 tiles split 8 ways along K); (c) a
-# ragged tail in M, N and K.
+# ------------------------------------------------------------------------------------------ stream-K
+# A dense launch whose tiles do not divide evenly over the resident CTAs (pairs)
+# runs the tiles of its last, partial wave as stream-K pieces: their k-blocks
+# are cut into equal ranges, one per unit, run before the unit's whole tiles;
+# the last piece of a tile to finish adds the fp32 partials in k order.
+# Shapes below: (a) more tiles than resident pairs, with a small remainder
+# (2304^2: 81 pair tiles on 76 pairs, 5 tiles in 20 pieces); (b) fewer tiles
+# than CTAs (512^2 x 2048: 8 tiles in 64 pieces); (c) a ragged tail in M, N
+# and K; (d) pieces of up to four per tile after three full waves (4096^2 x
+# 1024 with B column-major, the layout of the 4096^3 workload).
 
-SPLIT_SHAPES = [(2304, 2304, 1024), (512, 512, 2048), (1000, 776, 1480)]
+SPLIT_SHAPES = [(2304, 2304, 1024), (512, 512, 2048), (1000, 776, 1480), (4096, 4096, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
 @pytest.mark.parametrize("epi", ["none", "bias_gelu"])
-def test_split_tail_matches_oracle(M, N, K, epi):
-    case = wl.dense_random(M, N, K, seed=41, dist="normal", epi=epi)
+def test_stream_k_matches_oracle(M, N, K, epi):
+    case = wl.dense_random(M, N, K, seed=41, dist="normal", epi=epi, b_col_major=(M == 4096))
     c = run_dense(case)
     _sync_ok()
-    check_dense(case, c)
+    if M * N > 4_000_000:
+        check_dense(case, c, rows=sample_rows(M, 256, 160, seed=5))
+    else:
+        check_dense(case, c)
 
 
 @pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
-def test_split_tail_deterministic_and_close_to_unsplit(c_dtype, monkeypatch):
+def test_stream_k_deterministic_and_close_to_whole_tiles(c_dtype, monkeypatch):
     case = wl.dense_random(2304, 2304, 1024, seed=42, dist="normal", c_dtype=c_dtype, epi="bias")
     c1 = run_dense(case)
     c2 = run_dense(case)
-    monkeypatch.setenv("TG_SPLIT_TAIL", "0")
+    monkeypatch.setenv("TG_STREAM_K", "0")
     c0 = run_dense(case)
     _sync_ok()
-    assert torch.equal(c1, c2), "split tiles must not depend on which slice finishes last"
+    assert torch.equal(c1, c2), "stream-K tiles must not depend on which piece finishes last"
     check_dense(case, c0)
     check_dense(case, c1)
 
 
-def test_split_tail_integer_exact_bitwise():
-    # integer partial sums are exact in fp32, so the split result equals the exact one
-    for M, N, K in SPLIT_SHAPES:
+def test_stream_k_integer_exact_bitwise():
+    # integer partial sums are exact in fp32, so the stream-K result equals the exact one
+    for M, N, K in SPLIT_SHAPES[:3]:
         case = wl.dense_random(M, N, K, seed=43, dist="int4", c_dtype="f32", **lds(M, N, K, False, False))
         y, _ = oracle_dense(case)
         c = run_dense(case)
@@ -578,13 +603,9 @@ def test_split_tail_integer_exact_bitwise():
 
 
 @pytest.mark.parametrize("tile_shape", TILES)
-@pytest.mark.parametrize("mode", ["auto", "k"])
-def test_split_tail_every_variant(tile_shape, mode, monkeypatch):
-    # 640x520x1536: fewer tiles than CTAs; 2304^2 x 1024: one or two full waves and a
-    # remainder (column halves for 256-wide tiles, K-ranges for 128-wide or forced)
+def test_stream_k_every_variant(tile_shape, monkeypatch):
+    # 640x520x1536: fewer tiles than CTAs; 2304^2 x 1024: one or two full waves and a remainder
     monkeypatch.setenv("TG_TILE", tile_shape)
-    if mode == "k":
-        monkeypatch.setenv("TG_SPLIT_TAIL", "k")
     for M, N, K in [(640, 520, 1536), (2304, 2304, 1024)]:
         for a_col, b_col in LAYOUTS:
             case = wl.dense_random(M, N, K, seed=44, dist="uniform", a_col_major=a_col, b_col_major=b_col,
@@ -594,16 +615,22 @@ def test_split_tail_every_variant(tile_shape, mode, monkeypatch):
             check_dense(case, c)
 
 
-def test_split_tail_k_ranges_after_full_waves(monkeypatch):
-    # K-cut of the remainder after a full wave: deterministic, integer-exact
-    monkeypatch.setenv("TG_SPLIT_TAIL", "k")
-    case = wl.dense_random(2304, 2304, 1024, seed=45, dist="int4", c_dtype="f32")
-    y, _ = oracle_dense(case)
-    c1 = run_dense(case)
-    c2 = run_dense(case)
-    _sync_ok()
-    assert torch.equal(c1, c2)
-    assert np.array_equal(to_f64(c1), y)
+def test_stream_k_after_full_waves_integer_exact(monkeypatch):
+    # four pieces per tile after three full waves (the 4096^3 workload's plan at K = 1024):
+    # deterministic and integer-exact, f32 and bf16 output
+    for c_dtype in ("f32", "bf16"):
+        case = wl.dense_random(4096, 4096, 1024, seed=45, dist="int4", c_dtype=c_dtype, b_col_major=True)
+        rows = sample_rows(4096, 256, 64, seed=6)
+        y, _ = oracle_dense(case, rows=rows)
+        c1 = run_dense(case)
+        c2 = run_dense(case)
+        _sync_ok()
+        assert torch.equal(c1, c2)
+        got = to_f64(c1[torch.as_tensor(rows, device=c1.device)])
+        if c_dtype == "f32":
+            assert np.array_equal(got, y)
+        else:
+            assert np.array_equal(got, to_f64(torch.from_numpy(y).to(torch.bfloat16)))
 
 
 # ------------------------------------------------------------------------------------------ full-size workloads
