@@ -382,7 +382,12 @@ def debug_withhold_stage(k_block: int, block: int = 0) -> None:
 def debug_trace(tile_records: torch.Tensor | None, cta_records: torch.Tensor | None = None) -> None:
     """Arm a timeline trace of this thread's next launch (see tg_debug_trace in include/tg.h).
 
-    ``tile_records`` is an int64 CUDA tensor [T, 4] and ``cta_records`` [B, 4]."""
+    ``tile_records`` is an int64 CUDA tensor [T, 4] and ``cta_records`` [B, 4]; the
+    capacities passed to the library are T and B records of four stamps each."""
+    for name, t in (("tile_records", tile_records), ("cta_records", cta_records)):
+        if t is not None and (t.dim() != 2 or t.shape[1] != 4 or t.dtype != torch.int64 or not t.is_contiguous()
+                              or not t.is_cuda):
+            raise ValueError(f"{name} must be a contiguous int64 CUDA tensor of shape [n, 4]")
     tp = 0 if tile_records is None else tile_records.data_ptr()
     tc = 0 if tile_records is None else tile_records.shape[0]
     cp = 0 if cta_records is None else cta_records.data_ptr()

@@ -41,6 +41,7 @@ using tg::Params;
 using tg::Problem;
 
 constexpr uint32_t kDefaultBudgetMs = 1000;
+constexpr uint32_t kDefaultSleepNs = 20000;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
@@ -421,8 +422,20 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
 
 // Launch-wide fields every launch carries: the error record, the wait budget,
 // and the test and trace hooks armed on this thread (consumed by this launch).
+// Suspend hint of the producer's and epilogue's barrier waits, in ns (TG_SLEEP_NS
+// overrides it for tuning sweeps; 0 spins).
+uint32_t sleep_ns() {
+    static const uint32_t v = [] {
+        const char* env = std::getenv("TG_SLEEP_NS");
+        const long x = env ? std::strtol(env, nullptr, 10) : -1;
+        return (x >= 0 && x <= 1000000) ? static_cast<uint32_t>(x) : kDefaultSleepNs;
+    }();
+    return v;
+}
+
 void base_params(Params* p, tg::ErrorRecord* err) {
     p->err = err;
+    p->sleep_ns = sleep_ns();
     p->wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
     p->withhold_kb = t_withhold.kb;
     p->withhold_block = t_withhold.block;
@@ -437,7 +450,7 @@ void base_params(Params* p, tg::ErrorRecord* err) {
 // Launch with one CTA (pair) per work unit that has work: every resident unit,
 // or fewer when there are fewer whole tiles plus stream-K ranges than units.
 tg_status enqueue(const Params& p, const Variant& v, int units, cudaStream_t stream) {
-    int64_t want = p.total_tiles - p.sk_tiles;
+    int64_t want = p.total_tiles + p.nh_tiles - p.sk_tiles;
     if (p.sk_units > want) want = p.sk_units;
     if (want > units) want = units;
     const int grid = static_cast<int>(want) * v.cta_group;
@@ -561,12 +574,33 @@ tg_status tg_gemm_ex(const tg_group_problem* problem, tg_stream_t stream) {
 
 namespace {
 
-// Stream-K plan of a dense launch (tg::sk_plan); TG_STREAM_K=0 in the
-// environment turns it off (every tile in one piece, as grouped launches).
-tg::SkPlan plan_stream_k(int64_t tiles, int units, int k_blocks) {
+// The last, partial wave of a dense launch.  With T tiles on U units, its
+// R = T mod U tiles would leave U - R units idle.  Short tiles (at most
+// kHalvesMaxKb k-blocks) of 256 columns, when 2R <= U, run as 2R column halves:
+// a half costs 3/4 of a whole tile's operand bytes (the A box and half of B) and
+// needs no partial sums.  Longer tiles are balanced with stream-K (tg::sk_plan),
+// whose partial sums cost relatively less.  TG_STREAM_K=0 turns both off (one
+// unit per tile, as grouped launches); TG_STREAM_K=1 uses stream-K wherever its
+// plan applies.
+constexpr int kHalvesMaxKb = 96;
+
+struct WavePlan {
+    int64_t halves = 0;   // tiles run as column halves
+    tg::SkPlan sk;
+};
+
+WavePlan plan_last_wave(int64_t tiles, int units, int k_blocks, int bn) {
+    WavePlan wp;
     const char* env = std::getenv("TG_STREAM_K");
-    if (env && env[0] == '0') return tg::SkPlan{};
-    return tg::sk_plan(tiles, units, k_blocks);
+    if (env && env[0] == '0') return wp;
+    const bool force_sk = env && env[0] == '1';
+    const int64_t R = units > 0 ? tiles % units : 0;
+    if (!force_sk && bn == 256 && tiles > units && R > 0 && 2 * R <= units && k_blocks <= kHalvesMaxKb) {
+        wp.halves = R;
+        return wp;
+    }
+    wp.sk = tg::sk_plan(tiles, units, k_blocks);
+    return wp;
 }
 
 tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
@@ -599,14 +633,28 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
     base_params(&p, d->err);
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const tg::SkPlan sp = plan_stream_k(tiles, units, p.dense.k_blocks);
+    const WavePlan wp = plan_last_wave(tiles, units, p.dense.k_blocks, v.bn);
+    const tg::SkPlan& sp = wp.sk;
+    if (wp.halves > 0) {
+        p.nh_tiles = static_cast<int32_t>(wp.halves);
+        if (layout_b == TG_COL_MAJOR) {
+            // K-major B: a second map whose box covers the half of each CTA's N rows
+            const CUtensorMapDataType bt =
+                q.ab == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+            if ((s = make_map(&p.b_half, bt, q.B, q.K, q.N, q.ldb * 2, 64, v.bn_cta / 2, "B (column halves)", 0)) !=
+                TG_OK)
+                return s;
+        }
+    }
     void* ws = nullptr;
     int n_counters = 0;
     if (sp.tiles > 0) {
         // partial sums of every piece, then one arrival counter per (tile, CTA, epilogue warp)
+        // and one ready flag per (tile, piece, CTA, epilogue warp), all zeroed before the GEMM
         const size_t partial =
             static_cast<size_t>(sp.tiles) * sp.max_slices * v.tile_m * v.bn * sizeof(float);
-        n_counters = sp.tiles * v.cta_group * tg::NUM_EPI_WARPS;
+        const int n_count = sp.tiles * v.cta_group * tg::NUM_EPI_WARPS;
+        n_counters = n_count * (1 + sp.max_slices);
         cudaMemPool_t pool = nullptr;
         if ((s = device_pool(d, &pool)) != TG_OK) return s;
         cudaError_t e = cudaMallocFromPoolAsync(&ws, partial + n_counters * sizeof(uint32_t), pool, st);
@@ -616,6 +664,7 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
         p.sk_max_slices = sp.max_slices;
         p.sk_partial = static_cast<float*>(ws);
         p.sk_count = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + partial);
+        p.sk_flag = p.sk_count + n_count;
     }
     // the kernel before the GEMM: the row pass (which also zeroes the counters) or the counter reset;
     // the GEMM follows it as a programmatic dependent and waits for it only where it reads its output

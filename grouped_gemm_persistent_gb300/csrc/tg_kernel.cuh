@@ -112,12 +112,16 @@ enum : uint32_t {
 
 struct Params {
     Problem dense;              // the problem of a dense launch (lives in parameter space)
+    // Dense column halves (nh_tiles): B map whose box covers half the N rows of
+    // dense.tma_b's (K-major B); N-major B loads half as many 64-column boxes instead.
+    CUtensorMap b_half;
     const Problem* problems;    // grouped launch: device array written by the host
     int32_t num_problems;
     int32_t band;               // raster band width in N-tiles
     int64_t total_tiles;        // tiles of the launch (dense broadcast form: tiles x replicas)
     ErrorRecord* err;
     uint64_t wait_budget_ns;
+    uint32_t sleep_ns;          // suspend hint of the producer's and epilogue's barrier waits
     int64_t withhold_kb;        // test hook, -1 = off (see tg_debug_withhold_stage_in)
     int32_t withhold_block;
     // Timeline trace (tg_debug_trace), null when off.  trace_tiles[s] = {block,
@@ -146,11 +150,18 @@ struct Params {
     // tiles [0, sk_tiles), in tile order, are cut into sk_units contiguous ranges, range
     // r = [sk_bound(r), sk_bound(r + 1)) belonging to unit r.  Tiles [sk_tiles,
     // total_tiles) are whole tiles: unit u takes sk_tiles + u, sk_tiles + u + U, ...
+    // Column halves (dense only; exclusive with stream-K).  The last nh_tiles tiles, the
+    // last partial wave, each run as two units of BN/2 columns (N = BN/2 MMAs on half the
+    // B bytes; no partial sums): unit u's item index g = u, u + U, ... covers whole tile g
+    // while g < total_tiles - nh_tiles, then column half (g - f) / nh_tiles of tile
+    // f + (g - f) % nh_tiles, f = total_tiles - nh_tiles, for g < total_tiles + nh_tiles.
+    int32_t nh_tiles;
     int32_t sk_tiles;           // 0: no stream-K
     int32_t sk_units;
     int32_t sk_max_slices;      // pieces of one tile at most (stride of the partial slabs)
     float* sk_partial;          // [sk_tiles][sk_max_slices][CTA_GROUP][4 warps][BN/4][32 lanes][4]
     uint32_t* sk_count;         // [sk_tiles][CTA_GROUP][4 warps], zero at launch
+    uint32_t* sk_flag;          // [sk_tiles][sk_max_slices][CTA_GROUP][4 warps], zero at launch
 };
 
 // ----------------------------------------------------------------------------------------
@@ -209,9 +220,13 @@ __host__ __device__ __forceinline__ SkPiece sk_piece(int64_t cur, int64_t end, i
 // unit is busy with its next tile).  A piece costs a write of its fp32 partial
 // sums, so there is no stream-K when the pieces would be almost whole tiles
 // (R > 3 units / 4), when a range would hold a whole tile (U <= R), or when
-// k_blocks < 2 * SK_QUANTUM.
+// tiles are short: k_blocks < 2 * SK_QUANTUM, or, when units also run whole
+// tiles, k_blocks < SK_MIN_KB_WITH_WHOLE (a short tile's piece saves less than
+// its partial sums cost the units around it; measured on the 131072 x 128 x 1024
+// workload, 16 k-blocks per tile: 55 us without stream-K, 71 us with it).
 constexpr int SK_MAX_PIECES = 8;
 constexpr int SK_MAX_PIECES_WITH_WHOLE = 2;
+constexpr int SK_MIN_KB_WITH_WHOLE = 32;
 
 struct SkPlan {
     int tiles = 0;        // R: tiles [0, R) run as stream-K pieces (0: no stream-K)
@@ -224,7 +239,7 @@ __host__ __forceinline__ SkPlan sk_plan(int64_t tiles, int64_t units, int64_t k_
     if (units <= 1 || k_blocks < 2 * SK_QUANTUM || tiles <= 0) return sp;
     const int64_t R = tiles < units ? tiles : tiles % units;
     if (R == 0) return sp;
-    if (tiles > units && R * 4 > units * 3) return sp;
+    if (tiles > units && (R * 4 > units * 3 || k_blocks < SK_MIN_KB_WITH_WHOLE)) return sp;
     const int64_t total = R * k_blocks;
     int64_t U = units;
     const int64_t max_pieces = tiles > units ? SK_MAX_PIECES_WITH_WHOLE : SK_MAX_PIECES;
@@ -312,6 +327,9 @@ struct TileCoord {
     // columns [0, BN/2) in TMEM lanes 0-63 and [BN/2, BN) in lanes 64-127, both in
     // TMEM columns [0, BN/2).
     bool half;
+    // Column half (dense): columns [n0, n0 + BN/2) only, by N = BN/2 MMAs; the
+    // accumulator holds them in TMEM columns [0, BN/2) with the usual row layout.
+    bool nhalf;
 };
 
 // Device-counts MoE schedule, built in shared memory by every CTA at start:
@@ -367,6 +385,7 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
     TileCoord c;
     c.g = g;
     c.half = false;
+    c.nhalf = false;
     if constexpr (Cfg::CTA_GROUP == 2 && (Cfg::GROUPED || Cfg::MOE)) {
         const int rows_left = (Cfg::MOE ? mt.row_off[g + 1] - mt.row_off[g] : pr.M) - mb * Cfg::TILE_M;
         c.half = rows_left <= BM;
@@ -389,6 +408,7 @@ struct Work {
     int kb1;
     int slice;    // piece: its index among the tile's pieces (k order)
     int slices;   // piece: pieces of the tile (>= 2); 0 for a whole tile
+    int nh;       // column half (0 or 1), or -1
     int64_t slot; // i * U + u for the i-th item of unit u (trace index)
 };
 
@@ -426,6 +446,7 @@ __device__ __forceinline__ bool sched_next(const Params& p, int64_t unit, int64_
         if (s.cur < s.end && (s.i > 0 || s.next_tile >= total_tiles)) {
             const int kbs = p.dense.k_blocks;
             const SkPiece q = sk_piece(s.cur, s.end, kbs, p.sk_units, static_cast<int64_t>(p.sk_tiles) * kbs, unit);
+            w.nh = -1;
             w.t = q.t;
             w.kb0 = q.kb0;
             w.kb1 = q.kb1;
@@ -436,8 +457,18 @@ __device__ __forceinline__ bool sched_next(const Params& p, int64_t unit, int64_
             return true;
         }
     }
-    if (s.next_tile >= total_tiles) return false;
-    w.t = s.next_tile;
+    w.nh = -1;
+    int64_t whole = total_tiles;
+    if constexpr (!Cfg::GROUPED && !Cfg::MOE) whole -= p.nh_tiles;
+    if (s.next_tile >= whole) {
+        if constexpr (Cfg::GROUPED || Cfg::MOE) return false;
+        const int64_t hu = s.next_tile - whole;          // column-half unit
+        if (hu >= 2 * static_cast<int64_t>(p.nh_tiles)) return false;
+        w.t = whole + hu % p.nh_tiles;
+        w.nh = static_cast<int>(hu / p.nh_tiles);
+    } else {
+        w.t = s.next_tile;
+    }
     w.kb0 = 0;
     w.kb1 = 0;
     w.slice = 0;
@@ -445,6 +476,16 @@ __device__ __forceinline__ bool sched_next(const Params& p, int64_t unit, int64_
     s.next_tile += num_units;
     ++s.i;
     return true;
+}
+
+// The coordinates of a work item: its tile's, narrowed to one column half.
+template <class Cfg>
+__device__ __forceinline__ TileCoord coord_of(const Params& p, const Work& w, int g, uint32_t rank,
+                                              const MoeTable& mt) {
+    TileCoord c = tile_coord<Cfg>(p, w.t, g, rank, mt);
+    c.nhalf = w.nh >= 0;
+    if (c.nhalf) c.n0 += w.nh * (Cfg::BN / 2);
+    return c;
 }
 
 // k-blocks [begin, end) of a work item on problem pr
@@ -488,17 +529,18 @@ __device__ __forceinline__ bool abort_raised(uint32_t abort_addr) {
 // another role aborted; the caller leaves its loop.
 //
 // SLEEP waiters (everyone but the MMA issuer) let the hardware suspend them
-// inside try_wait until the phase completes (up to SLEEP_NS per call): a
-// spinning warp would take issue slots from the MMA-issuing warp on the same
-// SM sub-partition and leave the tensor pipe idle between instructions.
-constexpr uint32_t SLEEP_NS = 20000;
-
+// inside try_wait until the phase completes (up to p.sleep_ns per call; 0: no
+// suspend hint): a spinning warp would take issue slots from the MMA-issuing
+// warp on the same SM sub-partition and leave the tensor pipe idle between
+// instructions.
 template <int CTA_GROUP, bool SLEEP = true>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& p, uint32_t abort_addr,
                                              uint32_t role, int64_t tile, uint32_t stage) {
     auto try_once = [&]() {
-        if constexpr (SLEEP) return ptx::mbar_try_wait_sleep(bar, parity, SLEEP_NS);
-        else return ptx::mbar_try_wait(bar, parity);
+        if constexpr (SLEEP) {
+            if (p.sleep_ns) return ptx::mbar_try_wait_sleep(bar, parity, p.sleep_ns);
+        }
+        return ptx::mbar_try_wait(bar, parity);
     };
     if (try_once()) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
@@ -755,8 +797,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             bool aborted = false;
             bool maps_ready = !Cfg::MOE;   // MoE: the per-expert maps come from the kernel before this one
             bool withhold = (p.withhold_kb >= 0) && blockIdx.x == static_cast<uint32_t>(p.withhold_block);
-            // bytes each CTA loads per k-block; the leader's full barrier expects both CTAs'
-            constexpr uint32_t cta_tx = Cfg::A_BYTES + Cfg::B_BYTES;
             Sched sc = sched_begin<Cfg>(p, unit);
             Work w;
             while (!aborted && sched_next<Cfg>(p, unit, num_units, total_tiles, sc, w)) {
@@ -769,8 +809,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         g_fenced = g;
                     }
                 }
-                const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
-                const int nb0 = tc.n0 + static_cast<int>(rank) * Cfg::BN_CTA;   // first B column this CTA loads
+                const TileCoord tc = coord_of<Cfg>(p, w, g, rank, mt);
+                // first B column this CTA loads (a column half: half of each CTA's share)
+                const int nb0 = tc.n0 + static_cast<int>(rank) * (tc.nhalf ? Cfg::BN_CTA / 2 : Cfg::BN_CTA);
+                const int b_boxes = tc.nhalf ? Cfg::BN_CTA / 128 : Cfg::BN_CTA / 64;   // N-major B: 64-column boxes
+                const uint32_t item_tx = Cfg::A_BYTES + (tc.nhalf ? Cfg::B_BYTES / 2 : Cfg::B_BYTES);
                 const int kb_end = work_kb_end(w, pr);
                 // A rows: the problem's map at row m0, or (MoE) the expert's own map at its local row
                 const CUtensorMap* map_a = &pr.tma_a;
@@ -795,7 +838,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     const bool skip = withhold && kb == p.withhold_kb;
                     if (!skip) {
                         const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
-                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), cta_tx * CG);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), item_tx * CG);
                         const int k0 = kb * BK;
                         const uint32_t a_dst = sA + stage * Cfg::A_BYTES;
                         const uint32_t b_dst = sB + stage * Cfg::B_BYTES;
@@ -822,12 +865,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                             }
                         } else if constexpr (Cfg::B_MN) {
 #pragma unroll
-                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
+                                if (j < b_boxes) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+                        } else if constexpr (!Cfg::GROUPED) {
+                            load(b_dst, tc.nhalf ? &p.b_half : &pr.tma_b, k0, nb0);
                         } else {
                             load(b_dst, &pr.tma_b, k0, nb0);
                         }
                         st_shared_u32(base + Cfg::OFF_DRAIN_LAST + 4 * stage, pos);
-                        st_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * stage, cta_tx);
+                        st_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * stage, item_tx);
                     }
                     ++pos;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -878,9 +924,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 g = find_problem<Cfg>(p, w.t, g, mt);
                 const Problem& pr = problem_of<Cfg>(p, g);
                 // half tiles: M = 128 for the pair (bits 24-28 of the instruction descriptor hold M >> 4)
-                const TileCoord tcm = tile_coord<Cfg>(p, w.t, g, rank, mt);
+                // column halves: N = BN/2 (bits 17-22 hold N >> 3)
+                const TileCoord tcm = coord_of<Cfg>(p, w, g, rank, mt);
                 uint32_t idesc = pr.idesc;
                 if (tcm.half) idesc = (idesc & ~(0x1Fu << 24)) | ((128u >> 4) << 24);
+                if (tcm.nhalf) idesc = (idesc & ~(0x3Fu << 17)) | ((static_cast<uint32_t>(BN / 2) >> 3) << 17);
                 if (!warp_wait(tempty_bar(acc), acc_phase ^ 1u, w.slot, 16 + acc)) {
                     aborted = true;
                     break;
@@ -952,6 +1000,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
         int sbuf = 0;
         int g = 0, g_fenced = -1;
         bool maps_ready = !Cfg::MOE;
+        const uint64_t pol_c = ptx::l2_policy_evict_first();    // C is written once
         Sched sc = sched_begin<Cfg>(p, unit);
         Work w;
         while (sched_next<Cfg>(p, unit, num_units, total_tiles, sc, w)) {
@@ -970,7 +1019,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     g_fenced = g;
                 }
             }
-            const TileCoord tc = tile_coord<Cfg>(p, w.t, g, rank, mt);
+            const TileCoord tc = coord_of<Cfg>(p, w, g, rank, mt);
             // half tiles: warps q and q + 2 share rows (q % 2) * 32 .. + 32 of this CTA's 64,
             // warp q / 2 == 1 taking columns [BN/2, BN)
             const int row0 = tc.m0 + (tc.half ? (q % 2) * 32 : q * 32);
@@ -1017,19 +1066,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
 
             const uint32_t t_acc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
             constexpr int CHUNKS = BN / Cfg::CW;
-            const int n_chunks = tc.half ? CHUNKS / 2 : CHUNKS;
+            const int n_chunks = (tc.half || tc.nhalf) ? CHUNKS / 2 : CHUNKS;
 
             // accumulator columns [c * CW, (c + 1) * CW) of this lane's row; the last chunk
             // hands the TMEM buffer back to the MMA issuer
             auto read_chunk = [&](int c, float (&v)[Cfg::CW], bool release) {
                 if (has_acc && active) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int h = 0; h < Cfg::CW / 32; ++h) {
-                        ptx::tmem_ld_32x32b_x32(t_acc + c * Cfg::CW + h * 32, r);
+                    if constexpr (Cfg::CW == 64) {
+                        uint32_t r[64];
+                        ptx::tmem_ld_32x32b_x64(t_acc + c * Cfg::CW, r);
                         ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(r[i]);
+                        for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+                    } else {
+                        uint32_t r[32];
+                        ptx::tmem_ld_32x32b_x32(t_acc + c * Cfg::CW, r);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
                     }
                 } else {
 #pragma unroll
@@ -1122,7 +1176,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         const int j1 = static_cast<int>(static_cast<int64_t>(tc.r + 1) * pr.repeat / pr.replicas);
                         for (int j = j0; j < j1; ++j) ptx::tma_store_3d(&pr.tma_c, buf, n_chunk, j, row0);
                     } else {
-                        ptx::tma_store_2d(map_c, buf, n_chunk, row0 - c_row_base);
+                        ptx::tma_store_2d_hint(map_c, buf, n_chunk, row0 - c_row_base, pol_c);
                     }
                     ptx::bulk_commit_group();
                 }
@@ -1137,140 +1191,183 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     finish_chunk(c, v);
                 }
             } else {
-                // Stream-K piece: this warp's 32 x BN partial sums go to its own slab,
-                // float4 [column / 4][lane] so that a warp's stores are 512 contiguous bytes.
+                // Stream-K piece.  Each epilogue warp first arrives on the tile's counter (zeroed
+                // by the kernel launched just before this one).  Every piece but the last to
+                // arrive writes its 32 x BN partial sums to its own slab - float4 [column / 4]
+                // [lane], so that a warp's stores are 512 contiguous bytes - and raises its ready
+                // flag; the last one adds all S in k order, its own from TMEM, the others from
+                // their slabs once their flags are up.  Those pieces have arrived, so they are
+                // already writing and the wait ends (it is bounded all the same).
                 const int S = w.slices;
                 constexpr int64_t SLAB = 32 * BN;
                 auto slab = [&](int slice) {
                     return reinterpret_cast<float4*>(
                         p.sk_partial + (((w.t * p.sk_max_slices + slice) * CG + rank) * 4 + q) * SLAB);
                 };
-                float4* mine = slab(w.slice);
-                // the accumulator stays in TMEM until it is known whether this piece adds up
-#pragma unroll 1
-                for (int c = 0; c < CHUNKS; ++c) {
-                    float v[Cfg::CW];
-                    read_chunk(c, v, false);
-                    if (active) {
-#pragma unroll
-                        for (int i = 0; i < Cfg::CW / 4; ++i)
-                            __stcg(mine + (c * (Cfg::CW / 4) + i) * 32 + lane,
-                                   make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
-                    }
-                }
+                auto flag = [&](int slice) {
+                    return p.sk_flag + ((w.t * p.sk_max_slices + slice) * CG + rank) * 4 + q;
+                };
                 uint32_t last = 0;
                 if (active) {
-                    // publish: every lane's stores, then one arrival per warp
-                    __threadfence();
-                    __syncwarp();
                     if (lane == 0) {
                         ptx::grid_dependency_wait();   // the counters were zeroed by the kernel before this one
-                        const uint32_t idx = (static_cast<uint32_t>(w.t) * CG + rank) * 4 + q;
+                        const int64_t idx = (w.t * CG + rank) * 4 + q;
                         last = atomicAdd(p.sk_count + idx, 1u) == static_cast<uint32_t>(S - 1) ? 1u : 0u;
                     }
                     last = __shfl_sync(0xffffffffu, last, 0);
                 }
-                // the unit's last work item: its operand ring is idle from here on
-                Sched peek = sc;
-                Work after;
-                const bool unit_done = !sched_next<Cfg>(p, unit, num_units, total_tiles, peek, after);
-                if (last && unit_done) {
-                    // Every piece's partials are visible.  Add all S in k order, this piece's own
-                    // from TMEM (the same values it stored).  The others stream through this warp's
-                    // share of the operand ring - idle, as no MMA or load of this unit is left - with
-                    // cp.async, FIX_BUFS chunks in flight; each lane copies and reads back only its
-                    // own float4s.
-                    __threadfence();
-                    constexpr int CH_BYTES = 32 * Cfg::CW * 4;
-                    const uint32_t region = sA + static_cast<uint32_t>(q) * FIX_BUFS * CH_BYTES;
-                    const int items = CHUNKS * (S - 1);      // (chunk, other piece), chunk-major
-                    auto issue = [&](int k) {
-                        if (k < items) {
-                            const int c = k / (S - 1), j = k % (S - 1);
-                            const float4* src = slab(j < w.slice ? j : j + 1) + c * (Cfg::CW / 4) * 32 + lane;
-                            const uint32_t dst = region + static_cast<uint32_t>(k % FIX_BUFS) * CH_BYTES + lane * 16u;
-#pragma unroll
-                            for (int i = 0; i < Cfg::CW / 4; ++i) ptx::cp_async_16(dst + i * 512u, src + i * 32);
-                        }
-                        ptx::cp_async_commit();              // empty groups keep the count uniform
-                    };
-#pragma unroll 1
-                    for (int k = 0; k < FIX_BUFS - 1; ++k) issue(k);
-                    int k = 0;
+                if (!last) {
+                    // write the partial sums, hand the accumulator back, then raise the flag
+                    float4* mine = slab(w.slice);
 #pragma unroll 1
                     for (int c = 0; c < CHUNKS; ++c) {
                         float v[Cfg::CW];
-#pragma unroll 1
-                        for (int sl = 0; sl < S; ++sl) {
-                            float x[Cfg::CW];
-                            if (sl == w.slice) {
-                                read_chunk(c, x, c == CHUNKS - 1);
-                            } else {
-                                ptx::cp_async_wait<FIX_BUFS - 2>();   // item k has landed
-                                const uint32_t buf = region + static_cast<uint32_t>(k % FIX_BUFS) * CH_BYTES + lane * 16u;
+                        read_chunk(c, v, true);
+                        if (active) {
 #pragma unroll
-                                for (int i = 0; i < Cfg::CW / 4; ++i) {
-                                    const float4 y = ptx::ld_shared_f4(buf + i * 512u);
-                                    x[4 * i] = y.x;
-                                    x[4 * i + 1] = y.y;
-                                    x[4 * i + 2] = y.z;
-                                    x[4 * i + 3] = y.w;
-                                }
-                                issue(k + FIX_BUFS - 1);          // into the buffer of item k - 1
-                                ++k;
-                            }
-                            if (sl == 0) {
-#pragma unroll
-                                for (int i = 0; i < Cfg::CW; ++i) v[i] = x[i];
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < Cfg::CW; ++i) v[i] += x[i];
-                            }
+                            for (int i = 0; i < Cfg::CW / 4; ++i)
+                                __stcg(mine + (c * (Cfg::CW / 4) + i) * 32 + lane,
+                                       make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
                         }
-                        finish_chunk(c, v);
                     }
-                    ptx::cp_async_wait<0>();
-                } else if (last) {
-                    // Every piece's partials are visible.  Add all S in k order, this piece's own
-                    // from TMEM (the same values it stored), the others from L2; the operand ring
-                    // belongs to the unit's next work item, so they come straight into registers.
-                    __threadfence();
-#pragma unroll 1
-                    for (int c = 0; c < CHUNKS; ++c) {
-                        float v[Cfg::CW];
-#pragma unroll 1
-                        for (int sl = 0; sl < S; ++sl) {
-                            float x[Cfg::CW];
-                            if (sl == w.slice) {
-                                read_chunk(c, x, c == CHUNKS - 1);
-                            } else {
-                                const float4* src = slab(sl) + c * (Cfg::CW / 4) * 32 + lane;
-#pragma unroll
-                                for (int i = 0; i < Cfg::CW / 4; ++i) {
-                                    const float4 y = __ldcg(src + i * 32);
-                                    x[4 * i] = y.x;
-                                    x[4 * i + 1] = y.y;
-                                    x[4 * i + 2] = y.z;
-                                    x[4 * i + 3] = y.w;
-                                }
-                            }
-                            if (sl == 0) {
-#pragma unroll
-                                for (int i = 0; i < Cfg::CW; ++i) v[i] = x[i];
-                            } else {
-#pragma unroll
-                                for (int i = 0; i < Cfg::CW; ++i) v[i] += x[i];
-                            }
-                        }
-                        finish_chunk(c, v);
+                    if (active) {
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) ptx::st_release_gpu_u32(flag(w.slice), 1u);
                     }
                 } else {
-                    // not the last piece (or no rows here): hand the accumulator back
-                    ptx::tc_fence_before_sync();
-                    __syncwarp();
+                    // the other pieces' flags (each one's partials are then visible)
+                    uint32_t ok = 1;
                     if (lane == 0) {
-                        if (CG == 2 && !leader) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
-                        else ptx::mbar_arrive(tempty_bar(acc));
+                        const uint64_t t0 = ptx::globaltimer_ns();
+                        for (int sl = 0; sl < S && ok; ++sl) {
+                            if (sl == w.slice) continue;
+                            while (ptx::ld_acquire_gpu_u32(flag(sl)) == 0u) {
+                                const uint64_t dt = ptx::globaltimer_ns() - t0;
+                                if (dt > p.wait_budget_ns || abort_raised(abort_addr)) {
+                                    if (dt > p.wait_budget_ns) {
+                                        report_timeout(p, ROLE_EPILOGUE, w.slot, static_cast<uint32_t>(sl), dt);
+                                        raise_abort<CG>(abort_addr);
+                                    }
+                                    ok = 0;
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    __threadfence();
+                    // the unit's last work item: its operand ring is idle from here on
+                    Sched peek = sc;
+                    Work after;
+                    const bool unit_done = !sched_next<Cfg>(p, unit, num_units, total_tiles, peek, after);
+                    if (unit_done) {
+                        // The others stream through this warp's share of the operand ring - idle, as
+                        // no MMA or load of this unit is left - with cp.async, FIX_BUFS chunks in
+                        // flight; each lane copies and reads back only its own float4s.
+                        constexpr int CH_BYTES = 32 * Cfg::CW * 4;
+                        const uint32_t region = sA + static_cast<uint32_t>(q) * FIX_BUFS * CH_BYTES;
+                        const int items = CHUNKS * (S - 1);      // (chunk, other piece), chunk-major
+                        auto issue = [&](int k) {
+                            if (k < items) {
+                                const int c = k / (S - 1), j = k % (S - 1);
+                                const float4* src = slab(j < w.slice ? j : j + 1) + c * (Cfg::CW / 4) * 32 + lane;
+                                const uint32_t dst = region + static_cast<uint32_t>(k % FIX_BUFS) * CH_BYTES + lane * 16u;
+#pragma unroll
+                                for (int i = 0; i < Cfg::CW / 4; ++i) ptx::cp_async_16(dst + i * 512u, src + i * 32);
+                            }
+                            ptx::cp_async_commit();              // empty groups keep the count uniform
+                        };
+#pragma unroll 1
+                        for (int k = 0; k < FIX_BUFS - 1; ++k) issue(k);
+                        int k = 0;
+#pragma unroll 1
+                        for (int c = 0; c < CHUNKS; ++c) {
+                            float v[Cfg::CW];
+#pragma unroll 1
+                            for (int sl = 0; sl < S; ++sl) {
+                                float x[Cfg::CW];
+                                if (sl == w.slice) {
+                                    read_chunk(c, x, c == CHUNKS - 1);
+                                } else {
+                                    ptx::cp_async_wait<FIX_BUFS - 2>();   // item k has landed
+                                    const uint32_t buf = region + static_cast<uint32_t>(k % FIX_BUFS) * CH_BYTES + lane * 16u;
+#pragma unroll
+                                    for (int i = 0; i < Cfg::CW / 4; ++i) {
+                                        const float4 y = ptx::ld_shared_f4(buf + i * 512u);
+                                        x[4 * i] = y.x;
+                                        x[4 * i + 1] = y.y;
+                                        x[4 * i + 2] = y.z;
+                                        x[4 * i + 3] = y.w;
+                                    }
+                                    issue(k + FIX_BUFS - 1);          // into the buffer of item k - 1
+                                    ++k;
+                                }
+                                if (sl == 0) {
+#pragma unroll
+                                    for (int i = 0; i < Cfg::CW; ++i) v[i] = x[i];
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < Cfg::CW; ++i) v[i] += x[i];
+                                }
+                            }
+                            finish_chunk(c, v);
+                        }
+                        ptx::cp_async_wait<0>();
+                    } else {
+                        // The operand ring belongs to the unit's next work item: the others come
+                        // into registers, 32 columns at a time, the next (chunk, half, other piece)
+                        // item always in flight while the current one is added and the chunk stored.
+                        constexpr int HALVES = Cfg::CW / 32;
+                        const int items = CHUNKS * HALVES * (S - 1);
+                        float4 nx[8];
+                        auto load_item = [&](int k) {
+                            const int j = k % (S - 1), ch = k / (S - 1);
+                            const float4* src = slab(j < w.slice ? j : j + 1) + ch * 8 * 32 + lane;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) nx[i] = __ldcg(src + i * 32);
+                        };
+                        load_item(0);
+                        int k = 0;
+#pragma unroll 1
+                        for (int c = 0; c < CHUNKS; ++c) {
+                            // v = sum of the pieces in k order, accumulated in place
+                            float v[Cfg::CW];
+#pragma unroll
+                            for (int h = 0; h < HALVES; ++h) {
+#pragma unroll 1
+                                for (int sl = 0; sl < S; ++sl) {
+                                    if (sl == w.slice) {
+                                        uint32_t r[32];
+                                        ptx::tmem_ld_32x32b_x32(t_acc + c * Cfg::CW + h * 32, r);
+                                        ptx::tmem_ld_wait();
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i)
+                                            v[h * 32 + i] = sl == 0 ? __uint_as_float(r[i]) : v[h * 32 + i] + __uint_as_float(r[i]);
+                                    } else {
+#pragma unroll
+                                        for (int i = 0; i < 8; ++i) {
+                                            const float4 y = nx[i];
+                                            v[h * 32 + 4 * i] = sl == 0 ? y.x : v[h * 32 + 4 * i] + y.x;
+                                            v[h * 32 + 4 * i + 1] = sl == 0 ? y.y : v[h * 32 + 4 * i + 1] + y.y;
+                                            v[h * 32 + 4 * i + 2] = sl == 0 ? y.z : v[h * 32 + 4 * i + 2] + y.z;
+                                            v[h * 32 + 4 * i + 3] = sl == 0 ? y.w : v[h * 32 + 4 * i + 3] + y.w;
+                                        }
+                                        if (++k < items) load_item(k);
+                                    }
+                                }
+                            }
+                            if (c == CHUNKS - 1) {
+                                // this piece's accumulator is fully read: hand it back
+                                ptx::tc_fence_before_sync();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    if (CG == 2 && !leader) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
+                                    else ptx::mbar_arrive(tempty_bar(acc));
+                                }
+                            }
+                            finish_chunk(c, v);
+                        }
                     }
                 }
             }

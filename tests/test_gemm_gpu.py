@@ -555,21 +555,29 @@ def test_timeline_trace_records_every_tile(tile):
 
 # ------------------------------------------------------------------------------------------ stream-K
 # A dense launch whose tiles do not divide evenly over the resident CTAs (pairs)
-# runs the tiles of its last, partial wave as stream-K pieces: their k-blocks
-# are cut into equal ranges, one per unit, run before the unit's whole tiles;
-# the last piece of a tile to finish adds the fp32 partials in k order.
+# balances the tiles of its last, partial wave.  Tiles of at most 96 k-blocks
+# and 256 columns run as column halves when there is room for them (next
+# section); otherwise, and always under TG_STREAM_K=1 as here, as stream-K
+# pieces: their k-blocks are cut into equal ranges, one per unit, run after the
+# unit's first whole tile; the last piece of a tile to arrive adds the fp32
+# partials in k order.
 # Shapes below: (a) more tiles than resident pairs, with a small remainder
-# (2304^2: 81 pair tiles on 76 pairs, 5 tiles in 20 pieces); (b) fewer tiles
-# than CTAs (512^2 x 2048: 8 tiles in 64 pieces); (c) a ragged tail in M, N
-# and K; (d) pieces of up to four per tile after three full waves (4096^2 x
-# 1024 with B column-major, the layout of the 4096^3 workload).
+# (2304^2 x 2048: 81 pair tiles on 76 pairs, 5 tiles in 10 pieces); (b) fewer
+# tiles than CTAs (512^2 x 2048: 8 tiles in 64 pieces); (c) a ragged tail in M,
+# N and K; (d) two pieces per tile after a full wave (4096^2 x 2048 with B
+# column-major, the 4096^3 workload's layout and plan: 28 tiles in 56 pieces).
 
-SPLIT_SHAPES = [(2304, 2304, 1024), (512, 512, 2048), (1000, 776, 1480), (4096, 4096, 1024)]
+SPLIT_SHAPES = [(2304, 2304, 2048), (512, 512, 2048), (1000, 776, 1480), (4096, 4096, 2048)]
+
+
+@pytest.fixture
+def stream_k(monkeypatch):
+    monkeypatch.setenv("TG_STREAM_K", "1")
 
 
 @pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
 @pytest.mark.parametrize("epi", ["none", "bias_gelu"])
-def test_stream_k_matches_oracle(M, N, K, epi):
+def test_stream_k_matches_oracle(M, N, K, epi, stream_k):
     case = wl.dense_random(M, N, K, seed=41, dist="normal", epi=epi, b_col_major=(M == 4096))
     c = run_dense(case)
     _sync_ok()
@@ -580,8 +588,8 @@ def test_stream_k_matches_oracle(M, N, K, epi):
 
 
 @pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
-def test_stream_k_deterministic_and_close_to_whole_tiles(c_dtype, monkeypatch):
-    case = wl.dense_random(2304, 2304, 1024, seed=42, dist="normal", c_dtype=c_dtype, epi="bias")
+def test_stream_k_deterministic_and_close_to_whole_tiles(c_dtype, stream_k, monkeypatch):
+    case = wl.dense_random(2304, 2304, 2048, seed=42, dist="normal", c_dtype=c_dtype, epi="bias")
     c1 = run_dense(case)
     c2 = run_dense(case)
     monkeypatch.setenv("TG_STREAM_K", "0")
@@ -592,7 +600,7 @@ def test_stream_k_deterministic_and_close_to_whole_tiles(c_dtype, monkeypatch):
     check_dense(case, c1)
 
 
-def test_stream_k_integer_exact_bitwise():
+def test_stream_k_integer_exact_bitwise(stream_k):
     # integer partial sums are exact in fp32, so the stream-K result equals the exact one
     for M, N, K in SPLIT_SHAPES[:3]:
         case = wl.dense_random(M, N, K, seed=43, dist="int4", c_dtype="f32", **lds(M, N, K, False, False))
@@ -603,10 +611,10 @@ def test_stream_k_integer_exact_bitwise():
 
 
 @pytest.mark.parametrize("tile_shape", TILES)
-def test_stream_k_every_variant(tile_shape, monkeypatch):
-    # 640x520x1536: fewer tiles than CTAs; 2304^2 x 1024: one or two full waves and a remainder
+def test_stream_k_every_variant(tile_shape, stream_k, monkeypatch):
+    # 640x520x1536: fewer tiles than CTAs; 2304^2 x 2048: one or two full waves and a remainder
     monkeypatch.setenv("TG_TILE", tile_shape)
-    for M, N, K in [(640, 520, 1536), (2304, 2304, 1024)]:
+    for M, N, K in [(640, 520, 1536), (2304, 2304, 2048)]:
         for a_col, b_col in LAYOUTS:
             case = wl.dense_random(M, N, K, seed=44, dist="uniform", a_col_major=a_col, b_col_major=b_col,
                                    epi="bias", **lds(M, N, K, a_col, b_col))
@@ -615,11 +623,11 @@ def test_stream_k_every_variant(tile_shape, monkeypatch):
             check_dense(case, c)
 
 
-def test_stream_k_after_full_waves_integer_exact(monkeypatch):
-    # four pieces per tile after three full waves (the 4096^3 workload's plan at K = 1024):
+def test_stream_k_after_full_waves_integer_exact(stream_k):
+    # two pieces per tile between whole tiles (the 4096^3 workload's plan at K = 2048):
     # deterministic and integer-exact, f32 and bf16 output
     for c_dtype in ("f32", "bf16"):
-        case = wl.dense_random(4096, 4096, 1024, seed=45, dist="int4", c_dtype=c_dtype, b_col_major=True)
+        case = wl.dense_random(4096, 4096, 2048, seed=45, dist="int4", c_dtype=c_dtype, b_col_major=True)
         rows = sample_rows(4096, 256, 64, seed=6)
         y, _ = oracle_dense(case, rows=rows)
         c1 = run_dense(case)
@@ -631,6 +639,46 @@ def test_stream_k_after_full_waves_integer_exact(monkeypatch):
             assert np.array_equal(got, y)
         else:
             assert np.array_equal(got, to_f64(torch.from_numpy(y).to(torch.bfloat16)))
+
+
+# ------------------------------------------------------------------------------------------ column halves
+# With 256-wide tiles of at most 96 k-blocks and room for twice the last wave's
+# tiles, each of those tiles runs as two 128-column units (N = 128 MMAs; B
+# column-major through a second tensor map whose box covers half the N rows,
+# B row-major through half of the 64-column boxes).  No partial sums: every
+# element is one unit's fp32 accumulation in k order, so the result is bitwise
+# equal to the whole-tile one.  Shapes: 2304^2 (81 pair tiles: 5 in halves);
+# 4096^2 (256 pair tiles: 28 in halves, the 4096^3 workload's plan); a ragged
+# 2500 x 2300 (90 tiles: 14 in halves, partial last rows and columns).
+
+HALF_SHAPES = [(2304, 2304, 1024), (4096, 4096, 1024), (2500, 2300, 1000)]
+
+
+@pytest.mark.parametrize("M,N,K", HALF_SHAPES)
+@pytest.mark.parametrize("a_col,b_col", LAYOUTS)
+def test_column_halves_match_oracle_and_whole_tiles(M, N, K, a_col, b_col, monkeypatch):
+    case = wl.dense_random(M, N, K, seed=46, dist="normal", a_col_major=a_col, b_col_major=b_col, epi="bias_gelu",
+                           **lds(M, N, K, a_col, b_col))
+    c_half = run_dense(case)
+    monkeypatch.setenv("TG_STREAM_K", "0")
+    c_whole = run_dense(case)
+    _sync_ok()
+    assert torch.equal(c_half.view(torch.int16), c_whole.view(torch.int16)), "halves differ from whole tiles"
+    check_dense(case, c_half, rows=sample_rows(M, 256, 96, seed=7) if M * N > 4_000_000 else None)
+
+
+def test_column_halves_integer_exact_and_guard_bands():
+    M, N, K = 2304, 2304, 1024
+    case = wl.dense_random(M, N, K, seed=47, dist="int4", c_dtype="f32", b_col_major=True)
+    y, _ = oracle_dense(case)
+    big = torch.full((M + 16, N + 24), float("inf"), dtype=torch.float32, device="cuda")
+    out = big[8:8 + M, 8:8 + N]
+    run_dense(case, out)
+    _sync_ok()
+    assert np.array_equal(to_f64(out), y)
+    mask = torch.ones_like(big, dtype=torch.bool)
+    mask[8:8 + M, 8:8 + N] = False
+    assert torch.isinf(big[mask]).all(), "a write landed outside C"
 
 
 # ------------------------------------------------------------------------------------------ full-size workloads
