@@ -359,6 +359,21 @@ __device__ __forceinline__ int find_problem(const Params& p, int64_t t, int g, c
     }
 }
 
+// Raster of one problem's tiles_m x tiles_n tiles: bands of `band` N-tiles, swept
+// one M-row of the band after another; odd bands run up the M-tiles, so that the
+// A rows of a band's last raster rows, still in L2, serve the next band's first.
+// Tile `local` (0 <= local < tiles_m * tiles_n) is M-tile mb, N-tile nb.
+__host__ __device__ __forceinline__ void raster(int64_t local, int tiles_m, int tiles_n, int band, int& mb, int& nb) {
+    const int64_t per_band = static_cast<int64_t>(tiles_m) * band;
+    const int b = static_cast<int>(local / per_band);
+    const int r = static_cast<int>(local - static_cast<int64_t>(b) * per_band);
+    const int n_first = b * band;
+    const int width = band < tiles_n - n_first ? band : tiles_n - n_first;
+    const int row = r / width;
+    mb = (b & 1) ? tiles_m - 1 - row : row;
+    nb = n_first + (r - row * width);
+}
+
 template <class Cfg>
 __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int g, uint32_t rank,
                                                 const MoeTable& mt = {}) {
@@ -374,14 +389,8 @@ __device__ __forceinline__ TileCoord tile_coord(const Params& p, int64_t t, int 
         replica = static_cast<int>(local % pr.replicas);
         local /= pr.replicas;
     }
-    const int band = p.band;
-    const int64_t per_band = static_cast<int64_t>(tiles_m) * band;
-    const int b = static_cast<int>(local / per_band);
-    const int r = static_cast<int>(local - static_cast<int64_t>(b) * per_band);
-    const int n_first = b * band;
-    const int width = min(band, pr.tiles_n - n_first);
-    const int mb = r / width;
-    const int nb = n_first + (r - mb * width);
+    int mb, nb;
+    raster(local, tiles_m, pr.tiles_n, p.band, mb, nb);
     TileCoord c;
     c.g = g;
     c.half = false;

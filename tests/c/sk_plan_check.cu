@@ -9,7 +9,9 @@
 //     the workspace the host allocates;
 //   - every whole tile is taken by exactly one unit;
 //   - ranges differ in length by at most SK_QUANTUM k-blocks plus the remainder
-//     that the last range takes.
+//     that the last range takes;
+//   - the tile raster (tg::raster) visits every (M-tile, N-tile) of a problem
+//     exactly once, for every band width.
 // Prints one line per failure and "OK <plans> <stream-K plans>" at the end;
 // exit status 1 on any failure.
 #include <cstdio>
@@ -93,6 +95,22 @@ int main() {
                 for (long long t = R; t < T; ++t)
                     if (taken[static_cast<size_t>(t)] != 1) { fail("whole tile coverage", T, U_all, KB, t, taken[static_cast<size_t>(t)]); break; }
             }
-    std::printf("%s %lld %lld\n", failures ? "FAILED" : "OK", plans, sk_plans);
+    // the raster visits every (M-tile, N-tile) of a problem exactly once
+    long long rasters = 0;
+    for (int tm = 1; tm <= 40; ++tm)
+        for (int tn = 1; tn <= 40; ++tn)
+            for (int band : {1, 2, 3, 4, 8, 16}) {
+                ++rasters;
+                std::vector<int> seen(static_cast<size_t>(tm * tn), 0);
+                for (long long l = 0; l < static_cast<long long>(tm) * tn; ++l) {
+                    int mb = -1, nb = -1;
+                    tg::raster(l, tm, tn, band, mb, nb);
+                    if (mb < 0 || mb >= tm || nb < 0 || nb >= tn) { fail("raster out of range", tm, tn, band, mb, nb); break; }
+                    seen[static_cast<size_t>(mb * tn + nb)]++;
+                }
+                for (int i = 0; i < tm * tn; ++i)
+                    if (seen[static_cast<size_t>(i)] != 1) { fail("raster coverage", tm, tn, band, i, seen[static_cast<size_t>(i)]); break; }
+            }
+    std::printf("%s %lld %lld %lld\n", failures ? "FAILED" : "OK", plans, sk_plans, rasters);
     return failures ? 1 : 0;
 }

@@ -33,5 +33,6 @@ def test_stream_k_pieces_partition_every_tile(tmp_path):
     assert r.returncode == 0, r.stdout + r.stderr
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and out.stdout.strip().startswith("OK"), out.stdout
-    _, plans, sk_plans = out.stdout.split()
+    _, plans, sk_plans, rasters = out.stdout.split()
     assert int(plans) > 30000 and int(sk_plans) > 10000     # the sweep exercised stream-K plans
+    assert int(rasters) == 40 * 40 * 6
