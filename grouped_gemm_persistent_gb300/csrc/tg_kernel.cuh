@@ -947,22 +947,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const int kb_begin = w.kb0;
                 const int kb_end = work_kb_end(w, pr);
                 const bool trace_unit = p.trace_tiles != nullptr && w.slot < p.trace_tiles_cap;
-                for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!warp_wait(full_bar(stage), phase, w.slot, stage)) {
-                        aborted = true;
-                        break;
-                    }
-                    ptx::tc_fence_after_sync();
-                    if (lane == 0 && kb == kb_begin && trace_unit) {
-                        p.trace_tiles[4 * w.slot + 0] = blockIdx.x;
-                        p.trace_tiles[4 * w.slot + 1] = ptx::globaltimer_ns();
-                    }
+                // The four MMAs of one k-block execute in 512 tensor cycles (256 x 256 x 64), and
+                // issuing them with their commit takes ~375 issue cycles; with the barrier check
+                // and the loop around it, one k-block per iteration came to ~575 cycles, which
+                // left the tensor pipe idle ~10 % of the time.  So each iteration handles two
+                // stages: one warp-wide check of both full barriers, eight MMAs, two commits.
+                auto issue_stage = [&](int st, bool first) {
                     // stage s starts s * BYTES further on: add (s * BYTES) >> 4 to the start-address field
-                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((stage * Cfg::A_BYTES) >> 4);
-                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((stage * Cfg::B_BYTES) >> 4);
+                    const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((st * Cfg::A_BYTES) >> 4);
+                    const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((st * Cfg::B_BYTES) >> 4);
                     // All lanes run the issue code; a guard predicate lets lane 0 alone issue.
                     // Branching on the lane and reconverging each k-block left the tensor pipe
-                    // idle for ~15 % of the main loop; without the branch it is busy ~93-95 %.
+                    // idle for ~15 % of the main loop.
 #pragma unroll
                     for (int kk = 0; kk < BK / UMMA_K; ++kk) {
                         // K-major: the next 16 K elements are 32 bytes further along the
@@ -970,11 +966,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
                         const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
                         ptx::mma_bf16_guarded<CG>(lane == 0, d_tmem, a_desc + a_off, b_desc + b_off, idesc,
-                                                  (kb > kb_begin || kk > 0) ? 1u : 0u);
+                                                  (!first || kk > 0) ? 1u : 0u);
                     }
-                    ptx::mma_commit_guarded<CG>(lane == 0, empty_bar(stage));
+                    ptx::mma_commit_guarded<CG>(lane == 0, empty_bar(st));
+                };
+                for (int kb = kb_begin; kb < kb_end;) {
+                    const bool two = kb + 1 < kb_end;
+                    const int stage2 = stage + 1 == STAGES ? 0 : stage + 1;
+                    const uint32_t phase2 = stage + 1 == STAGES ? phase ^ 1u : phase;
+                    const bool ready = __all_sync(0xffffffffu, ptx::mbar_try_wait(full_bar(stage), phase) &&
+                                                                   (!two || ptx::mbar_try_wait(full_bar(stage2), phase2)));
+                    if (!ready) {
+                        if (!warp_wait(full_bar(stage), phase, w.slot, stage) ||
+                            (two && !warp_wait(full_bar(stage2), phase2, w.slot, stage2))) {
+                            aborted = true;
+                            break;
+                        }
+                    }
+                    ptx::tc_fence_after_sync();
+                    if (lane == 0 && kb == kb_begin && trace_unit) {
+                        p.trace_tiles[4 * w.slot + 0] = blockIdx.x;
+                        p.trace_tiles[4 * w.slot + 1] = ptx::globaltimer_ns();
+                    }
+                    issue_stage(stage, kb == kb_begin);
+                    if (two) issue_stage(stage2, false);
                     any_mma = true;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    const int adv = two ? 2 : 1;
+                    kb += adv;
+                    stage += adv;
+                    if (stage >= STAGES) { stage -= STAGES; phase ^= 1u; }
                 }
                 if (aborted) break;
                 if (lane == 0) {
