@@ -208,6 +208,28 @@ tg_status make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, u
     return TG_OK;
 }
 
+// 4-D map [d3][d2][d1][inner] with strides (in bytes) for the three outer dimensions.
+tg_status make_map_4d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, const uint64_t dims_in[4],
+                      const uint64_t strides_in[3], const uint32_t box_in[4], const char* what) {
+    const cuuint64_t dims[4] = {dims_in[0], dims_in[1], dims_in[2], dims_in[3]};
+    const cuuint64_t strides[3] = {strides_in[0], strides_in[1], strides_in[2]};
+    const cuuint32_t box[4] = {box_in[0], box_in[1], box_in[2], box_in[3]};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, dt, 4, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TG_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, int(r));
+    return TG_OK;
+}
+
+// N-major B whose columns split into whole 64-column chunks can be read through the
+// wide view {64 columns, k, chunk}: the chunk stride is 128 bytes, so every element of
+// the view lies inside a row's first N columns (a ragged last chunk would not).
+bool wide_b_ok(tg_layout lb, int64_t N, int bn_cta) {
+    return lb == TG_ROW_MAJOR && N % 64 == 0 && bn_cta >= 128;
+}
+
 // ----------------------------------------------------------------------------------------
 // argument checks
 
@@ -392,7 +414,12 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
         else
             s = make_map(&out->tma_a, bf16, q.A, q.M, q.K, q.lda * 2, 64, 64, "A", g);
         if (s != TG_OK) return s;
-        if (q.lb == TG_ROW_MAJOR)
+        if (wide_b_ok(q.lb, q.N, v.bn_cta)) {
+            // one box per k-block: {64 columns, 64 k, the CTA's BN_CTA / 64 chunks}
+            s = make_map_3d(&out->tma_b, bf16, q.B, 64, q.K, q.N / 64, q.ldb * 2, 128, 64, 64, v.bn_cta / 64,
+                            "B (64-column chunks)");
+            out->flags |= tg::FLAG_B_WIDE;
+        } else if (q.lb == TG_ROW_MAJOR)
             s = make_map(&out->tma_b, bf16, q.B, q.N, q.K, q.ldb * 2, 64, 64, "B", g);
         else
             s = make_map(&out->tma_b, bf16, q.B, q.K, q.N, q.ldb * 2, 64, v.bn_cta, "B", g);
@@ -407,7 +434,7 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
     out->bias = q.epi != TG_EPI_NONE ? q.bias : nullptr;
     out->row_scale = q.row_scale;
     out->idesc = tg::ptx::idesc_f32_acc(v.tile_m, v.bn, q.la == TG_COL_MAJOR, q.lb == TG_ROW_MAJOR, ab_f16);
-    out->flags = (q.cd == TG_F16 ? tg::FLAG_C_F16 : 0u) | (ab_f16 ? tg::FLAG_BIAS_F16 : 0u);
+    out->flags |= (q.cd == TG_F16 ? tg::FLAG_C_F16 : 0u) | (ab_f16 ? tg::FLAG_BIAS_F16 : 0u);
     out->M = static_cast<int32_t>(q.M);
     out->N = static_cast<int32_t>(q.N);
     out->K = static_cast<int32_t>(q.K);
@@ -637,12 +664,16 @@ tg_status dense_gemm(const Prob& q, tg_stream_t stream, const RowPass* pre) {
     const tg::SkPlan& sp = wp.sk;
     if (wp.halves > 0) {
         p.nh_tiles = static_cast<int32_t>(wp.halves);
+        const CUtensorMapDataType bt =
+            q.ab == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         if (layout_b == TG_COL_MAJOR) {
             // K-major B: a second map whose box covers the half of each CTA's N rows
-            const CUtensorMapDataType bt =
-                q.ab == TG_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
             if ((s = make_map(&p.b_half, bt, q.B, q.K, q.N, q.ldb * 2, 64, v.bn_cta / 2, "B (column halves)", 0)) !=
                 TG_OK)
+                return s;
+        } else if (p.dense.flags & tg::FLAG_B_WIDE) {
+            // N-major B through the wide view: halves load 64-column boxes of the plain map
+            if ((s = make_map(&p.b_half, bt, q.B, q.N, q.K, q.ldb * 2, 64, 64, "B (column halves)", 0)) != TG_OK)
                 return s;
         }
     }
@@ -784,7 +815,16 @@ tg_status tg_moe_gemm(const void* A, int64_t lda, int64_t T, int64_t K, const vo
     if ((s = fill_problem(q, v, 0, &p.dense)) != TG_OK) return s;
     if (K > 0) {
         // B as one 3-D tensor: expert g is the outermost coordinate
-        if (layout_b == TG_ROW_MAJOR)
+        p.dense.flags &= ~tg::FLAG_B_WIDE;
+        if (wide_b_ok(layout_b, N, v.bn_cta)) {
+            const uint64_t dims[4] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64),
+                                      static_cast<uint64_t>(G)};
+            const uint64_t strides[3] = {static_cast<uint64_t>(ldb) * 2, 128, static_cast<uint64_t>(expert_stride) * 2};
+            const uint32_t box[4] = {64, 64, static_cast<uint32_t>(v.bn_cta / 64), 1};
+            s = make_map_4d(&p.dense.tma_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, dims, strides, box,
+                            "B (experts, 64-column chunks)");
+            p.dense.flags |= tg::FLAG_B_WIDE;
+        } else if (layout_b == TG_ROW_MAJOR)
             s = make_map_3d(&p.dense.tma_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, N, K, G, ldb * 2, expert_stride * 2,
                             64, 64, 1, "B (experts)");
         else

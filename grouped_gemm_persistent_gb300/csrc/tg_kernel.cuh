@@ -108,12 +108,18 @@ struct alignas(128) Problem {
 enum : uint32_t {
     FLAG_C_F16 = 1u,      // 16-bit output is IEEE fp16 (else bf16)
     FLAG_BIAS_F16 = 2u,   // bias is fp16 (else bf16)
+    // N-major B with N % 64 == 0: tma_b is the view {64 columns, k, column chunk of 64}
+    // (MoE: plus the expert), so a CTA's BN_CTA columns of one k-block are a single box.
+    // Each TMA instruction costs the producer about as much as a quarter of an MMA
+    // k-block, so one box instead of BN_CTA / 64 keeps the ring ahead of the MMA.
+    FLAG_B_WIDE = 4u,
 };
 
 struct Params {
     Problem dense;              // the problem of a dense launch (lives in parameter space)
     // Dense column halves (nh_tiles): B map whose box covers half the N rows of
-    // dense.tma_b's (K-major B); N-major B loads half as many 64-column boxes instead.
+    // dense.tma_b's (K-major B); N-major B loads half as many 64-column boxes instead,
+    // from this map (the plain 2-D one) when dense.tma_b is the wide view (FLAG_B_WIDE).
     CUtensorMap b_half;
     const Problem* problems;    // grouped launch: device array written by the host
     int32_t num_problems;
@@ -778,6 +784,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             ptx::prefetch_tensormap(&p.dense.tma_a);
             ptx::prefetch_tensormap(&p.dense.tma_b);
             ptx::prefetch_tensormap(&p.dense.tma_c);
+            if (p.nh_tiles > 0) ptx::prefetch_tensormap(&p.b_half);
         }
     }
     ptx::tc_fence_before_sync();
@@ -823,6 +830,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const int nb0 = tc.n0 + static_cast<int>(rank) * (tc.nhalf ? Cfg::BN_CTA / 2 : Cfg::BN_CTA);
                 const int b_boxes = tc.nhalf ? Cfg::BN_CTA / 128 : Cfg::BN_CTA / 64;   // N-major B: 64-column boxes
                 const uint32_t item_tx = Cfg::A_BYTES + (tc.nhalf ? Cfg::B_BYTES / 2 : Cfg::B_BYTES);
+                const bool b_wide = Cfg::B_MN && (pr.flags & FLAG_B_WIDE) != 0;
                 const int kb_end = work_kb_end(w, pr);
                 // A rows: the problem's map at row m0, or (MoE) the expert's own map at its local row
                 const CUtensorMap* map_a = &pr.tma_a;
@@ -839,18 +847,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         g_fenced = g;
                     }
                 }
-                for (int kb = w.kb0; kb < kb_end; ++kb) {
-                    if (!wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, w.slot, stage)) {
-                        aborted = true;
-                        break;
-                    }
+                // One k-block's loads into ring stage st (ring position `at`).
+                auto load_stage = [&](int st, int kb, uint32_t at) {
                     const bool skip = withhold && kb == p.withhold_kb;
                     if (!skip) {
-                        const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(stage), 0) : full_bar(stage);
-                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), item_tx * CG);
+                        const uint32_t fb = (CG == 2) ? ptx::mapa(full_bar(st), 0) : full_bar(st);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(st), item_tx * CG);
                         const int k0 = kb * BK;
-                        const uint32_t a_dst = sA + stage * Cfg::A_BYTES;
-                        const uint32_t b_dst = sB + stage * Cfg::B_BYTES;
+                        const uint32_t a_dst = sA + st * Cfg::A_BYTES;
+                        const uint32_t b_dst = sB + st * Cfg::B_BYTES;
                         auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y) {
                             if constexpr (CG == 2) ptx::tma_load_2d_pair(dst, m, x, y, fb);
                             else ptx::tma_load_2d(dst, m, x, y, fb);
@@ -867,25 +872,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                                 else ptx::tma_load_3d(dst, &pr.tma_b, x, y, tc.g, fb);
                             };
                             if constexpr (Cfg::B_MN) {
+                                if (b_wide) {
+                                    if constexpr (CG == 2) ptx::tma_load_4d_pair(b_dst, &pr.tma_b, 0, k0, nb0 / 64, tc.g, fb);
+                                    else ptx::tma_load_4d(b_dst, &pr.tma_b, 0, k0, nb0 / 64, tc.g, fb);
+                                } else {
 #pragma unroll
-                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load3(b_dst + j * 8192, nb0 + j * 64, k0);
+                                    for (int j = 0; j < Cfg::BN_CTA / 64; ++j) load3(b_dst + j * 8192, nb0 + j * 64, k0);
+                                }
                             } else {
                                 load3(b_dst, k0, nb0);
                             }
                         } else if constexpr (Cfg::B_MN) {
+                            if (b_wide && !tc.nhalf) {
+                                // box {64 columns, 64 k, BN_CTA / 64 chunks}: lands as the chunks' 8 KiB blocks in order
+                                if constexpr (CG == 2) ptx::tma_load_3d_pair(b_dst, &pr.tma_b, 0, k0, nb0 / 64, fb);
+                                else ptx::tma_load_3d(b_dst, &pr.tma_b, 0, k0, nb0 / 64, fb);
+                            } else {
+                                const CUtensorMap* mb = b_wide ? &p.b_half : &pr.tma_b;
 #pragma unroll
-                            for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
-                                if (j < b_boxes) load(b_dst + j * 8192, &pr.tma_b, nb0 + j * 64, k0);
+                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
+                                    if (j < b_boxes) load(b_dst + j * 8192, mb, nb0 + j * 64, k0);
+                            }
                         } else if constexpr (!Cfg::GROUPED) {
                             load(b_dst, tc.nhalf ? &p.b_half : &pr.tma_b, k0, nb0);
                         } else {
                             load(b_dst, &pr.tma_b, k0, nb0);
                         }
-                        st_shared_u32(base + Cfg::OFF_DRAIN_LAST + 4 * stage, pos);
-                        st_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * stage, item_tx);
+                        st_shared_u32(base + Cfg::OFF_DRAIN_LAST + 4 * st, at);
+                        st_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * st, item_tx);
                     }
-                    ++pos;
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                };
+                // Two ring stages per iteration, like the MMA issuer: one wait on the later
+                // stage's slot, then both stages' loads.  The MMA's commits complete in order,
+                // so the later slot being free means the earlier one is too.  A single thread
+                // issues every load of the CTA, and each wait on a barrier that has already
+                // completed still costs it ~130 cycles: at one wait per k-block it could not
+                // keep up with the MMA (512 tensor cycles per k-block).
+                for (int kb = w.kb0; kb < kb_end;) {
+                    const bool two = kb + 1 < kb_end;
+                    const int last = two ? (stage + 1 == STAGES ? 0 : stage + 1) : stage;
+                    const uint32_t last_phase = (two && stage + 1 == STAGES) ? phase ^ 1u : phase;
+                    if (!wait_bounded<CG>(empty_bar(last), last_phase ^ 1u, p, abort_addr, ROLE_PRODUCER, w.slot, last)) {
+                        aborted = true;
+                        break;
+                    }
+                    load_stage(stage, kb, pos);
+                    if (two) load_stage(last, kb + 1, pos + 1u);
+                    const int adv = two ? 2 : 1;
+                    kb += adv;
+                    pos += static_cast<uint32_t>(adv);
+                    stage += adv;
+                    if (stage >= STAGES) { stage -= STAGES; phase ^= 1u; }
                 }
                 withhold = false;
             }

@@ -197,6 +197,22 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
         :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(cluster_bar) : "memory");
 }
 
+// 4-D tiled load global -> own shared memory, completion on an mbarrier of this CTA.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar) : "memory");
+}
+
+// 4-D form of tma_load_2d_pair.
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 int32_t w, uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        :: "r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(cluster_bar) : "memory");
+}
+
 // 2-D tiled store own shared memory -> global (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"

@@ -681,6 +681,62 @@ def test_column_halves_integer_exact_and_guard_bands():
     assert torch.isinf(big[mask]).all(), "a write landed outside C"
 
 
+# ------------------------------------------------------------------------------------------ N-major B, wide view
+# N-major B with N % 64 == 0 is read through the view {64 columns, k, 64-column chunk}: one
+# TMA box per k-block for a CTA's share of the tile.  Chunks past N (a partial last
+# N-tile, or a CTA whose whole share lies past N) read as zeros.
+
+WIDE_SHAPES = [(333, 320, 200), (300, 640, 136), (257, 64, 520)]
+
+
+@pytest.mark.parametrize("M,N,K", WIDE_SHAPES)
+@pytest.mark.parametrize("a_col", [False, True])
+def test_wide_b_view_integer_exact(M, N, K, a_col, tile):
+    case = wl.dense_random(M, N, K, seed=M + N + K, dist="int4", a_col_major=a_col, b_col_major=False,
+                           c_dtype="f32", **lds(M, N, K, a_col, False))
+    y, _ = oracle_dense(case)
+    c = run_dense(case)
+    _sync_ok()
+    assert np.array_equal(to_f64(c), y)
+
+
+@pytest.mark.parametrize("epi,c_dtype", [("bias_gelu", "bf16"), ("none", "f32")])
+def test_wide_b_view_equals_plain_boxes_bitwise(epi, c_dtype, tile):
+    # N = 320 takes the wide view, N = 328 (not a multiple of 64) the 64-column boxes of the
+    # plain map; on the same A, B columns and bias the first 320 columns agree bit for bit
+    M, K, N = 333, 200, 328
+    case = wl.dense_random(M, N, K, seed=48, dist="normal", epi=epi, c_dtype=c_dtype)
+    a, b, bias = to_device(case.a), to_device(case.b), to_device(case.bias) if case.bias is not None else None
+    dt = torch.float32 if c_dtype == "f32" else torch.bfloat16
+    wide = torch.empty((M, 320), dtype=dt, device="cuda")
+    plain = torch.empty((M, N), dtype=dt, device="cuda")
+    tg.gemm(a, b[:, :320], wide, bias=None if bias is None else bias[:320], epilogue=epi)
+    tg.gemm(a, b, plain, bias=bias, epilogue=epi)
+    _sync_ok()
+    iv = torch.int32 if c_dtype == "f32" else torch.int16
+    assert torch.equal(wide.view(iv), plain[:, :320].contiguous().view(iv))
+    check_dense(case, plain)
+
+
+@pytest.mark.parametrize("c_dtype", [torch.bfloat16, torch.float32])
+def test_wide_b_view_grouped_and_moe(c_dtype, tile):
+    # the host-table grouped form (a wide 3-D view per problem) and the device-counts MoE
+    # form (one 4-D view over all experts) on the same problems: bitwise equal, and parity
+    counts = [0, 300, 5, 0, 130, 257, 1, 0, 64]
+    case, a, b, bias, T = _moe_case(counts, 320, 200, 54, epi="bias_gelu", extra_rows=8)
+    dev = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    out_dev = torch.full((T, 320), float("nan"), dtype=c_dtype, device="cuda")
+    tg.moe_gemm_device(a, b, dev, out_dev, bias=bias, epilogue="bias_gelu")
+    used = int(sum(counts))
+    out_tab = torch.full((used, 320), float("nan"), dtype=c_dtype, device="cuda")
+    tg.moe_grouped_gemm(a[:used], b, counts, out_tab, bias=bias, epilogue="bias_gelu")
+    _sync_ok()
+    iv = torch.int32 if c_dtype == torch.float32 else torch.int16
+    assert torch.equal(out_dev[:used].view(iv), out_tab.view(iv))
+    assert torch.isnan(out_dev[used:].float()).all(), "rows past the counts were written"
+    _check_grouped(case, out_dev[:used])
+
+
 # ------------------------------------------------------------------------------------------ full-size workloads
 
 def test_workload_dense_4096_bias_gelu_full():
