@@ -41,7 +41,6 @@ using tg::Params;
 using tg::Problem;
 
 constexpr uint32_t kDefaultBudgetMs = 1000;
-constexpr uint32_t kDefaultSleepNs = 20000;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
@@ -449,20 +448,8 @@ tg_status fill_problem(const Prob& q, const Variant& v, int g, Problem* out) {
 
 // Launch-wide fields every launch carries: the error record, the wait budget,
 // and the test and trace hooks armed on this thread (consumed by this launch).
-// Suspend hint of the producer's and epilogue's barrier waits, in ns (TG_SLEEP_NS
-// overrides it for tuning sweeps; 0 spins).
-uint32_t sleep_ns() {
-    static const uint32_t v = [] {
-        const char* env = std::getenv("TG_SLEEP_NS");
-        const long x = env ? std::strtol(env, nullptr, 10) : -1;
-        return (x >= 0 && x <= 1000000) ? static_cast<uint32_t>(x) : kDefaultSleepNs;
-    }();
-    return v;
-}
-
 void base_params(Params* p, tg::ErrorRecord* err) {
     p->err = err;
-    p->sleep_ns = sleep_ns();
     p->wait_budget_ns = static_cast<uint64_t>(budget_ms()) * 1000000ull;
     p->withhold_kb = t_withhold.kb;
     p->withhold_block = t_withhold.block;

@@ -127,7 +127,6 @@ struct Params {
     int64_t total_tiles;        // tiles of the launch (dense broadcast form: tiles x replicas)
     ErrorRecord* err;
     uint64_t wait_budget_ns;
-    uint32_t sleep_ns;          // suspend hint of the producer's and epilogue's barrier waits
     int64_t withhold_kb;        // test hook, -1 = off (see tg_debug_withhold_stage_in)
     int32_t withhold_block;
     // Timeline trace (tg_debug_trace), null when off.  trace_tiles[s] = {block,
@@ -544,18 +543,19 @@ __device__ __forceinline__ bool abort_raised(uint32_t abort_addr) {
 // another role aborted; the caller leaves its loop.
 //
 // SLEEP waiters (everyone but the MMA issuer) let the hardware suspend them
-// inside try_wait until the phase completes (up to p.sleep_ns per call; 0: no
-// suspend hint): a spinning warp would take issue slots from the MMA-issuing
-// warp on the same SM sub-partition and leave the tensor pipe idle between
-// instructions.
+// inside try_wait until the phase completes (up to SLEEP_NS per call): a
+// spinning warp would take issue slots from the MMA-issuing warp on the same
+// SM sub-partition and leave the tensor pipe idle between instructions.  The
+// hint is an immediate: taken from a kernel parameter instead, the main loops
+// of the N-major-B GEMMs ran ~1 % slower per k-block.
+constexpr uint32_t SLEEP_NS = 20000;
+
 template <int CTA_GROUP, bool SLEEP = true>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Params& p, uint32_t abort_addr,
                                              uint32_t role, int64_t tile, uint32_t stage) {
     auto try_once = [&]() {
-        if constexpr (SLEEP) {
-            if (p.sleep_ns) return ptx::mbar_try_wait_sleep(bar, parity, p.sleep_ns);
-        }
-        return ptx::mbar_try_wait(bar, parity);
+        if constexpr (SLEEP) return ptx::mbar_try_wait_sleep(bar, parity, SLEEP_NS);
+        else return ptx::mbar_try_wait(bar, parity);
     };
     if (try_once()) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
@@ -985,10 +985,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const int kb_end = work_kb_end(w, pr);
                 const bool trace_unit = p.trace_tiles != nullptr && w.slot < p.trace_tiles_cap;
                 // The four MMAs of one k-block execute in 512 tensor cycles (256 x 256 x 64), and
-                // issuing them with their commit takes ~375 issue cycles; with the barrier check
-                // and the loop around it, one k-block per iteration came to ~575 cycles, which
-                // left the tensor pipe idle ~10 % of the time.  So each iteration handles two
-                // stages: one warp-wide check of both full barriers, eight MMAs, two commits.
+                // issuing them with their commit takes ~375 issue cycles.  With K-major B, one
+                // k-block per iteration (barrier check, loop) came to ~575 cycles a k-block, so
+                // there each iteration handles two stages: one warp-wide check of both full
+                // barriers, eight MMAs, two commits.  With N-major B the operand ring, not the
+                // issue loop, sets the pace, and waiting for two stages before issuing made the
+                // 8192^3 and MoE main loops slower (~585 against ~555 cycles a k-block).
+                constexpr bool PAIRS = !Cfg::B_MN;
                 auto issue_stage = [&](int st, bool first) {
                     // stage s starts s * BYTES further on: add (s * BYTES) >> 4 to the start-address field
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((st * Cfg::A_BYTES) >> 4);
@@ -1008,7 +1011,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                     ptx::mma_commit_guarded<CG>(lane == 0, empty_bar(st));
                 };
                 for (int kb = kb_begin; kb < kb_end;) {
-                    const bool two = kb + 1 < kb_end;
+                    const bool two = PAIRS && kb + 1 < kb_end;
                     const int stage2 = stage + 1 == STAGES ? 0 : stage + 1;
                     const uint32_t phase2 = stage + 1 == STAGES ? phase ^ 1u : phase;
                     const bool ready = __all_sync(0xffffffffu, ptx::mbar_try_wait(full_bar(stage), phase) &&
