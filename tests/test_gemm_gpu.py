@@ -770,3 +770,13 @@ def test_workload_grouped_moe_sampled():
     assert not torch.isnan(out.float()).any()
     rows = [sample_rows(int(m), 256, 24, seed=g) if m else np.zeros(0, np.int64) for g, m in enumerate(case.counts)]
     _check_grouped(case, out, rows_per_group=rows)
+
+
+def test_trace_summary_of_a_small_launch():
+    # the trace module's summary of a real traced launch: one unit per tile, times ordered
+    from grouped_gemm_persistent_gb300 import trace
+    out = trace.trace("dense_256", reps=1)
+    d = out[0]
+    assert d["units"] == 2 and d["pairs"] == 2                 # 2 single-CTA 128x256 tiles
+    assert d["span_us"] > 0 and d["ramp_us"][0] > 0 and d["final_epi_us"][0] > 0
+    assert 0.0 <= d["idle_tail_share"] < 1.0 and 0.0 < d["busy_share"] <= 1.0
