@@ -37,13 +37,17 @@
  *  - Degenerate sizes: M == 0 or N == 0 is a no-op returning TG_OK.  K == 0
  *    is the empty sum: C = epilogue(0), i.e. zeros, bias, or GELU(bias).
  *  - Results are deterministic: two identical calls write bitwise-identical C.
- *    A dense call whose tiles do not divide evenly over the SMs runs stream-K:
- *    the k-blocks of the tiles of its last, partial wave are cut into equal
- *    ranges, one per CTA (pair), which run first; the fp32 partial sums of a
- *    tile's pieces are added in k order (an atomic counter only picks which SM
- *    does the adding), so the result does not depend on timing.  Set
- *    TG_STREAM_K=0 in the environment to turn it off (one K order per tile, as
- *    grouped calls).
+ *    A dense call whose tiles do not divide evenly over the SMs runs the tiles
+ *    of its last, partial wave in smaller units.  Tiles of at most 96 k-blocks,
+ *    when there are at most half as many of them as CTA pairs, run as two
+ *    128-column halves (no partial sums: bitwise equal to whole tiles).  Other
+ *    last waves run as stream-K pieces: their k-blocks are cut into ranges of
+ *    equal length, one per CTA pair, each run after the pair's first whole
+ *    tile; the fp32 partial sums of a tile's pieces are added in k order (an
+ *    atomic counter only picks which SM does the adding), so the result does
+ *    not depend on timing.  TG_STREAM_K=0 in the environment runs whole tiles
+ *    only (one K order per tile, as grouped calls); TG_STREAM_K=1 uses stream-K
+ *    pieces where column halves would be chosen.
  *  - Dense stream-K calls take a workspace from a library-owned stream-ordered
  *    memory pool (up to 9 x 256 KiB per stream-K tile, fewer than the resident
  *    CTA pairs; released on the stream after the launch).
@@ -128,7 +132,7 @@ tg_status tg_gemm(const void *A, tg_layout layout_a, int64_t lda,
  * broadcasts inside the kernel.  Each distinct result row is computed once per
  * replica CTA and stored `repeat` times, so A costs U*K*2 bytes of traffic
  * instead of U*repeat*K*2.  Results are bitwise identical to tg_gemm on the
- * materialised A when that call runs without stream-K (always with
+ * materialised A when that call runs without stream-K pieces (always with
  * TG_STREAM_K=0), and within the stated tolerance otherwise.
  *
  *   A_user, layout_a, lda : bf16 U x K (row-major: lda >= K; column-major: lda >= U).
