@@ -230,6 +230,20 @@ def test_f16_integer_exact(tile):
     assert torch.equal(out16.cpu().view(torch.int16), torch.from_numpy(exact).to(torch.float16).view(torch.int16))
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.float32])
+def test_f16_wide_b_view_integer_exact(out_dtype, tile):
+    # fp16 operands with N-major B and N % 64 == 0 (the 64-column-chunk view of B), a
+    # partial last N-tile and a ragged K: integer inputs, so the result is exact
+    a, b, _ = _f16_case(333, 320, 200, 64, False, False, ints=True)
+    out = tg.gemm(a.cuda(), b.cuda(), out_dtype=out_dtype)
+    _sync_ok()
+    exact = (a.double() @ b.double()).numpy()
+    if out_dtype == torch.float32:
+        assert np.array_equal(to_f64(out), exact)
+    else:
+        assert torch.equal(out.cpu().view(torch.int16), torch.from_numpy(exact).to(torch.float16).view(torch.int16))
+
+
 def test_grouped_mixed_bf16_and_f16_problems(tile):
     gen = torch.Generator().manual_seed(63)
     keep, probs, refs = [], [], []
@@ -780,3 +794,44 @@ def test_trace_summary_of_a_small_launch():
     assert d["units"] == 2 and d["pairs"] == 2                 # 2 single-CTA 128x256 tiles
     assert d["span_us"] > 0 and d["ramp_us"][0] > 0 and d["final_epi_us"][0] > 0
     assert 0.0 <= d["idle_tail_share"] < 1.0 and 0.0 < d["busy_share"] <= 1.0
+
+
+# ------------------------------------------------------------------------------------------ extreme sizes
+
+def test_long_k_integer_exact():
+    # 1024 k-blocks: the operand ring laps ~170 times inside one tile; integer sums stay exact
+    M, N, K = 256, 320, 65536
+    case = wl.dense_random(M, N, K, seed=70, dist="int4", c_dtype="f32")
+    y, _ = oracle_dense(case)
+    c = run_dense(case)
+    _sync_ok()
+    assert np.array_equal(to_f64(c), y)
+
+
+def test_tall_skinny_many_tiles_sampled():
+    # 2344 M-tiles of one N-tile each: 30 rounds of the persistent schedule
+    M, N, K = 600_000, 64, 64
+    case = wl.dense_random(M, N, K, seed=71, dist="int4", c_dtype="f32")
+    rows = np.unique(np.concatenate([sample_rows(M, 256, 64, seed=9), np.arange(M - 300, M)]))
+    y, _ = oracle_dense(case, rows=rows)
+    c = run_dense(case)
+    _sync_ok()
+    assert np.array_equal(to_f64(c[torch.as_tensor(rows, device=c.device)]), y)
+
+
+def test_moe_device_counts_at_the_expert_limit():
+    # TG_MOE_MAX_EXPERTS experts, a fifth of them empty, ragged counts; bitwise equal to the
+    # host-table grouped GEMM and within the bound of the oracle
+    G = 190
+    rng = np.random.default_rng(72)
+    counts = rng.integers(0, 300, size=G)
+    counts[rng.choice(G, size=G // 5, replace=False)] = 0
+    case, a, b, bias, T = _moe_case(counts.tolist(), 128, 64, 72)
+    dev = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    out_dev = torch.full((T, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tg.moe_gemm_device(a, b, dev, out_dev)
+    out_tab = torch.empty_like(out_dev)
+    tg.moe_grouped_gemm(a, b, counts.tolist(), out_tab)
+    _sync_ok()
+    assert torch.equal(out_dev.view(torch.int16), out_tab.view(torch.int16))
+    _check_grouped(case, out_dev)
