@@ -12,7 +12,8 @@ to tg_grouped_gemm's on the same problems and, element by element, within the
 parity bound of the oracle's values.  The third call mixes layout and output
 classes (each class takes its own slice of the table and its own launch) and
 comes after a call with more problems, so an entry left over from the earlier
-call at a shifted offset would show up as a wrong result.
+call at a shifted offset would show up as a wrong result; the fourth has N a
+multiple of 64, so its row-major B problems take the 64-column-chunk view.
 
 The file is named so that pytest collects it last.
 """
@@ -58,7 +59,8 @@ def test_noalloc_matches_grouped_gemm_and_oracle_on_three_calls():
     mixed = [(False, torch.bfloat16), (True, torch.float32), (False, torch.float32), (True, torch.bfloat16)]
     sets = [([0, 300, 5, 0, 130, 257, 1, 0, 64, 17, 200], 136, 200, 41, "bias_gelu", row_bf16),  # empty first/middle/last
             ([64, 0, 513], 264, 128, 42, "none", row_bf16),                                 # fewer problems
-            ([33, 0, 129, 256, 7, 90], 200, 136, 43, "bias", mixed)]                       # four classes
+            ([33, 0, 129, 256, 7, 90], 200, 136, 43, "bias", mixed),                       # four classes
+            ([300, 0, 64, 129], 256, 128, 44, "bias_gelu", mixed)]                         # N-major B as 64-column chunks
     for counts, N, K, seed, epi, classes in sets:
         case, keep, t_ref, t_na, outs = _problems(counts, N, K, seed, epi, classes)
         assert lib.tg_grouped_gemm(t_ref, len(counts), stream) == tg.TG_OK, lib.tg_last_error_message()
