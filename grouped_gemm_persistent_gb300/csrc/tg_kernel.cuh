@@ -902,20 +902,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         st_shared_u32(base + Cfg::OFF_DRAIN_BYTES + 4 * st, item_tx);
                     }
                 };
-                // Two ring stages per iteration, like the MMA issuer: one wait on the later
-                // stage's slot, then both stages' loads.  The MMA's commits complete in order,
-                // so the later slot being free means the earlier one is too.  A single thread
-                // issues every load of the CTA, and each wait on a barrier that has already
-                // completed still costs it ~130 cycles: at one wait per k-block it could not
-                // keep up with the MMA (512 tensor cycles per k-block).
+                // One or two ring stages per iteration.  A slot is refilled as soon as the
+                // MMA releases it: the producer waits for this stage's slot alone (a
+                // non-blocking probe first, as a blocking wait on a barrier that has already
+                // completed still costs the single issuing thread ~130 cycles), then loads
+                // the next stage as well if its slot is already free.  Waiting for both
+                // slots before loading either, as an earlier form did, delayed every other
+                // refill by a k-block of MMA work; with 6 stages the ring's round trip
+                // has no slack for that (4 stages run at ~735 cycles a k-block).
                 for (int kb = w.kb0; kb < kb_end;) {
-                    const bool two = kb + 1 < kb_end;
-                    const int last = two ? (stage + 1 == STAGES ? 0 : stage + 1) : stage;
-                    const uint32_t last_phase = (two && stage + 1 == STAGES) ? phase ^ 1u : phase;
-                    if (!wait_bounded<CG>(empty_bar(last), last_phase ^ 1u, p, abort_addr, ROLE_PRODUCER, w.slot, last)) {
+                    const int last = stage + 1 == STAGES ? 0 : stage + 1;
+                    const uint32_t last_phase = stage + 1 == STAGES ? phase ^ 1u : phase;
+                    if (!ptx::mbar_test_wait(empty_bar(stage), phase ^ 1u) &&
+                        !wait_bounded<CG>(empty_bar(stage), phase ^ 1u, p, abort_addr, ROLE_PRODUCER, w.slot, stage)) {
                         aborted = true;
                         break;
                     }
+                    const bool two = kb + 1 < kb_end && ptx::mbar_test_wait(empty_bar(last), last_phase ^ 1u);
                     load_stage(stage, kb, pos);
                     if (two) load_stage(last, kb + 1, pos + 1u);
                     const int adv = two ? 2 : 1;
