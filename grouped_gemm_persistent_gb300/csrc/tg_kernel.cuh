@@ -8,8 +8,8 @@
 //
 //   warp 0      TMA producer: one thread streams A and B k-blocks into a
 //               STAGES-deep ring; full[s] completes when the bytes land.
-//   warp 1      MMA issuer: the converged warp waits full[s]; lane 0 alone (a
-//               guard predicate, no branch) issues BK/16 tcgen05.mma into TMEM
+//   warp 1      MMA issuer: the converged warp waits full[s]; one lane picked by
+//               elect.sync (no branch) issues BK/16 tcgen05.mma into TMEM
 //               accumulator buffer b and commits empty[s] (slot free) and,
 //               after the last k-block, tfull[b] (tile done).  Warp 1 also
 //               allocates and frees tensor memory.
@@ -1001,44 +1001,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                 const int kb_begin = w.kb0;
                 const int kb_end = work_kb_end(w, pr);
                 const bool trace_unit = p.trace_tiles != nullptr && w.slot < p.trace_tiles_cap;
-                // The four MMAs of one k-block execute in 512 tensor cycles (256 x 256 x 64), and
-                // issuing them with their commit takes ~375 issue cycles.  With K-major B, one
-                // k-block per iteration (barrier check, loop) came to ~575 cycles a k-block, so
-                // there each iteration handles two stages: one warp-wide check of both full
-                // barriers, eight MMAs, two commits.  With N-major B the operand ring, not the
-                // issue loop, sets the pace, and waiting for two stages before issuing made the
-                // 8192^3 and MoE main loops slower (~585 against ~555 cycles a k-block).
-                constexpr bool PAIRS = !Cfg::B_MN;
+                // One ring stage per iteration: a warp-wide check of its full barrier, then the
+                // stage's four MMAs and its commit from one elected lane.  The MMAs of a
+                // 256 x 256 x 64 k-block take 512 tensor cycles, and the elected issue of all
+                // five instructions takes fewer, so the loop keeps the pipe fed at every tile
+                // width.  (With a lane-0 guard on each instruction the issue took ~365 cycles,
+                // and K-major launches handled two stages per iteration to save a barrier
+                // check; with the elected issue that form measured ~1 % slower at 4096^3 and
+                // 3-6 % slower with N-major B.)
                 auto issue_stage = [&](int st, bool first) {
                     // stage s starts s * BYTES further on: add (s * BYTES) >> 4 to the start-address field
                     const uint64_t a_desc = a_desc0 + static_cast<uint64_t>((st * Cfg::A_BYTES) >> 4);
                     const uint64_t b_desc = b_desc0 + static_cast<uint64_t>((st * Cfg::B_BYTES) >> 4);
-                    // All lanes run the issue code; a guard predicate lets lane 0 alone issue.
-                    // Branching on the lane and reconverging each k-block left the tensor pipe
-                    // idle for ~15 % of the main loop.
-#pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // K-major: the next 16 K elements are 32 bytes further along the
-                        // swizzled row; MN-major: 16 rows (2048 bytes) further down.
-                        const uint64_t a_off = Cfg::A_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
-                        const uint64_t b_off = Cfg::B_MN ? (2048u * kk) >> 4 : (32u * kk) >> 4;
-                        ptx::mma_bf16_guarded<CG>(lane == 0, d_tmem, a_desc + a_off, b_desc + b_off, idesc,
-                                                  (!first || kk > 0) ? 1u : 0u);
-                    }
-                    ptx::mma_commit_guarded<CG>(lane == 0, empty_bar(st));
+                    // All lanes run the issue code and elect.sync picks the lane that issues
+                    // (branching on the lane and reconverging each k-block left the tensor pipe
+                    // idle for ~15 % of the main loop).  Step kk of the stage: K-major, the next
+                    // 16 K elements are 32 bytes further along the swizzled row; MN-major, 16
+                    // rows (2048 bytes) further down.
+                    static_assert(BK / UMMA_K == 4, "four MMAs per ring stage");
+                    constexpr uint64_t AO = Cfg::A_MN ? 2048u >> 4 : 32u >> 4;
+                    constexpr uint64_t BO = Cfg::B_MN ? 2048u >> 4 : 32u >> 4;
+                    ptx::mma_stage_elect<CG>(d_tmem, a_desc, a_desc + AO, a_desc + 2 * AO, a_desc + 3 * AO,
+                                             b_desc, b_desc + BO, b_desc + 2 * BO, b_desc + 3 * BO, idesc,
+                                             first ? 0u : 1u, empty_bar(st));
                 };
-                for (int kb = kb_begin; kb < kb_end;) {
-                    const bool two = PAIRS && kb + 1 < kb_end;
-                    const int stage2 = stage + 1 == STAGES ? 0 : stage + 1;
-                    const uint32_t phase2 = stage + 1 == STAGES ? phase ^ 1u : phase;
-                    const bool ready = __all_sync(0xffffffffu, ptx::mbar_try_wait(full_bar(stage), phase) &&
-                                                                   (!two || ptx::mbar_try_wait(full_bar(stage2), phase2)));
-                    if (!ready) {
-                        if (!warp_wait(full_bar(stage), phase, w.slot, stage) ||
-                            (two && !warp_wait(full_bar(stage2), phase2, w.slot, stage2))) {
-                            aborted = true;
-                            break;
-                        }
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if (!warp_wait(full_bar(stage), phase, w.slot, stage)) {
+                        aborted = true;
+                        break;
                     }
                     ptx::tc_fence_after_sync();
                     if (lane == 0 && kb == kb_begin && trace_unit) {
@@ -1046,12 +1036,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
                         p.trace_tiles[4 * w.slot + 1] = ptx::globaltimer_ns();
                     }
                     issue_stage(stage, kb == kb_begin);
-                    if (two) issue_stage(stage2, false);
                     any_mma = true;
-                    const int adv = two ? 2 : 1;
-                    kb += adv;
-                    stage += adv;
-                    if (stage >= STAGES) { stage -= STAGES; phase ^= 1u; }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (aborted) break;
                 if (lane == 0) {
