@@ -65,6 +65,7 @@ constexpr int FIX_BUFS = 4;          // chunks in flight per warp while a unit's
 constexpr int C_STAGE_BYTES = 32 * 128;   // per-warp store staging buffer: 32 rows x 128 bytes
 constexpr int SMEM_LIMIT = 232448;        // max dynamic shared memory per CTA on sm_100 family
 constexpr int MOE_MAX_G = 190;            // experts per call of the device-counts MoE form (table in shared memory)
+constexpr int GROUP_TABLE_MAX = 2 * (MOE_MAX_G + 1);   // grouped launches: problems whose first tiles fit that table
 constexpr int SK_QUANTUM = 4;             // stream-K range boundaries fall on multiples of 4 k-blocks
 constexpr int MAX_STAGES = 8;
 
@@ -281,16 +282,19 @@ struct Config {
     static constexpr int CW = C_F32 ? 32 : 64;       // output columns per 128-byte staged row
     static constexpr int TMEM_COLS = 2 * BN;         // two fp32 accumulators of BN columns
     static constexpr int C_BYTES = NUM_EPI_WARPS * 2 * C_STAGE_BYTES;
-    static constexpr int MOE_BYTES = MOE ? 8 * (MOE_MAX_G + 1) : 0;   // tile and row prefix sums
-    static constexpr int FIXED = C_BYTES + MOE_BYTES + 512 /*barriers and slots*/ + 1024 /*alignment slack*/;
+    // Prefix tables in shared memory: MoE, tiles and rows before each expert; grouped, each
+    // problem's first tile (while the problems fit), so that finding a unit's problem at a
+    // unit boundary reads no global memory.
+    static constexpr int TABLE_BYTES = (MOE || GROUPED) ? 8 * (MOE_MAX_G + 1) : 0;
+    static constexpr int FIXED = C_BYTES + TABLE_BYTES + 512 /*barriers and slots*/ + 1024 /*alignment slack*/;
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_C = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_MOE = OFF_C + C_BYTES;
-    static constexpr int OFF_BAR = OFF_MOE + MOE_BYTES;
+    static constexpr int OFF_TABLE = OFF_C + C_BYTES;
+    static constexpr int OFF_BAR = OFF_TABLE + TABLE_BYTES;
     // barriers: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + 8 * NUM_BARS;
@@ -339,9 +343,11 @@ struct TileCoord {
 
 // Device-counts MoE schedule, built in shared memory by every CTA at start:
 // tile_pref[g] = tiles of experts before g, row_off[g] = rows before g.
+// Shared-memory prefix tables (null when a launch has none).  MoE: tiles and rows before
+// each expert, [G + 1] each.  Grouped: tile_pref[i] = problem i's first tile.
 struct MoeTable {
-    const int32_t* tile_pref;   // [G + 1]
-    const int32_t* row_off;     // [G + 1]
+    const int32_t* tile_pref;
+    const int32_t* row_off;
 };
 
 template <class Cfg>
@@ -350,11 +356,23 @@ __device__ __forceinline__ const Problem& problem_of(const Params& p, int g) {
     else return p.dense;
 }
 
+// Grouped launches keep each problem's first tile in shared memory when the problems fit
+// the table and the tile indices fit 32 bits.
+__device__ __forceinline__ bool group_table_fits(const Params& p) {
+    return p.num_problems <= GROUP_TABLE_MAX && p.total_tiles <= 0x7fffffffll;
+}
+
 // Problem (or expert) containing global tile t; `g` is a hint that only moves forward.
+// Grouped: from the shared-memory table of first tiles when there is one (mt.tile_pref),
+// else from the problem array in global memory, one dependent load per problem passed.
 template <class Cfg>
 __device__ __forceinline__ int find_problem(const Params& p, int64_t t, int g, const MoeTable& mt = {}) {
     if constexpr (Cfg::GROUPED) {
-        while (g + 1 < p.num_problems && p.problems[g + 1].tile_begin <= t) ++g;
+        if (mt.tile_pref != nullptr) {
+            while (g + 1 < p.num_problems && mt.tile_pref[g + 1] <= t) ++g;
+        } else {
+            while (g + 1 < p.num_problems && p.problems[g + 1].tile_begin <= t) ++g;
+        }
         return g;
     } else if constexpr (Cfg::MOE) {
         while (g + 1 < p.moe_groups && mt.tile_pref[g + 1] <= t) ++g;
@@ -755,7 +773,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     if constexpr (Cfg::MOE) {
         if (warp == EPI_WARP0) {
             // Prefix sums of the device-resident token counts: rows and tiles before each expert.
-            int32_t* tile_pref = reinterpret_cast<int32_t*>(smem + Cfg::OFF_MOE);
+            int32_t* tile_pref = reinterpret_cast<int32_t*>(smem + Cfg::OFF_TABLE);
             int32_t* row_off = tile_pref + (MOE_MAX_G + 1);
             const int G = p.moe_groups;
             const int64_t tiles_n = p.dense.tiles_n;
@@ -793,6 +811,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
             }
         }
     }
+    if constexpr (Cfg::GROUPED) {
+        if (warp == EPI_WARP0 && group_table_fits(p)) {
+            int32_t* first_tile = reinterpret_cast<int32_t*>(smem + Cfg::OFF_TABLE);
+            for (int i = lane; i < p.num_problems; i += 32)
+                first_tile[i] = static_cast<int32_t>(p.problems[i].tile_begin);
+        }
+    }
     if constexpr (!Cfg::GROUPED) {
         if (threadIdx.x == 0) {
             ptx::prefetch_tensormap(&p.dense.tma_a);
@@ -809,8 +834,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_kernel(const __grid_const
     MoeTable mt{};
     if constexpr (Cfg::MOE) {
         total_tiles = *reinterpret_cast<volatile int32_t*>(smem + Cfg::OFF_MOE_TOTAL);
-        mt.tile_pref = reinterpret_cast<const int32_t*>(smem + Cfg::OFF_MOE);
+        mt.tile_pref = reinterpret_cast<const int32_t*>(smem + Cfg::OFF_TABLE);
         mt.row_off = mt.tile_pref + (MOE_MAX_G + 1);
+    }
+    if constexpr (Cfg::GROUPED) {
+        if (group_table_fits(p)) mt.tile_pref = reinterpret_cast<const int32_t*>(smem + Cfg::OFF_TABLE);
     }
     if (p.trace_ctas && threadIdx.x == 0 && blockIdx.x < p.trace_ctas_cap) {
         p.trace_ctas[4 * blockIdx.x + 0] = t_entry;

@@ -343,6 +343,23 @@ def test_grouped_ragged_with_empty_groups(epi, b_col, tile):
     _check_grouped(case, out, b_col=b_col)
 
 
+def test_grouped_more_problems_than_the_shared_table():
+    # The kernel keeps each problem's first tile in shared memory for up to 382
+    # problems and walks the problem array in global memory beyond that: 420
+    # non-empty problems (and a few empty ones) take the global walk.
+    rng = np.random.default_rng(31)
+    counts = [int(c) for c in rng.integers(1, 40, size=424)]
+    for i in (0, 100, 250, 423):
+        counts[i] = 0
+    case, a, b, out, bias = _grouped_problems(counts, 64, 64, 32, epi="bias")
+    sentinel = torch.full_like(out, float("nan"))
+    out.copy_(sentinel)
+    tg.moe_grouped_gemm(a, b, counts, out, bias=bias, epilogue="bias")
+    _sync_ok()
+    assert not torch.isnan(out.float()).any(), "a row of a non-empty group was not written"
+    _check_grouped(case, out)
+
+
 def test_grouped_single_group_matches_dense_bitwise(tile, monkeypatch):
     monkeypatch.setenv("TG_STREAM_K", "0")    # same summation order on both paths
     case = wl.dense_random(700, 392, 320, seed=22, dist="normal", epi="bias")
