@@ -112,18 +112,87 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# NVML clock-event reason bits (nvmlClocksEventReason*) for the reasons the line reports.
+NVML_REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                    "hw_thermal_slowdown": 0x40}
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def nvml_reason_flags(mask: int) -> list[str]:
+    """NVML's clock-event reason bit mask -> "Active" / "Not Active" per REASON_NAMES."""
+    return ["Active" if mask & NVML_REASON_BITS[n] else "Not Active" for n in REASON_NAMES]
+
+
+class _Nvml:
+    """Read-only NVML queries through the driver's own library (no Python package needed):
+    SM clock, its maximum, board power and the clock-event reasons of one device."""
+
+    def __init__(self, torch_index: int):
+        import ctypes
+        import torch
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        props = torch.cuda.get_device_properties(torch_index)
+        bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) != 0:
+            lib.nvmlShutdown()
+            raise OSError("no NVML device for " + bus.decode())
+        try:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self.reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct, lib, h = self.ct, self.lib, self.h
+        sm, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(sm)) != 0 or lib.nvmlDeviceGetMaxClockInfo(h, 1, ct.byref(mx)) != 0
+                or lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) != 0 or self.reasons_fn(h, ct.byref(rs)) != 0):
+            return None
+        return (float(sm.value), float(mx.value), mw.value / 1000.0, nvml_reason_flags(rs.value))
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 100 ms while running."""
+    """SM clock, power and throttle reasons sampled while the timed region runs: every ~2 ms
+    through NVML when the driver's library loads, else nvidia-smi every 100 ms (short timed
+    regions then catch few samples)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.nvml = None
+        self.rows = None
+        self.thread = None
+        self.stop = None
+
+    def _nvml_loop(self):
+        while not self.stop.is_set():
+            r = self.nvml.sample()
+            if r is not None:
+                self.rows.append(r)
+            time.sleep(self.PERIOD_S)
 
     def __enter__(self):
+        try:
+            import threading
+            self.nvml = _Nvml(self.gpu)
+            self.rows, self.stop = [], threading.Event()
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.thread.start()
+            return self
+        except (OSError, AttributeError, ImportError):
+            self.nvml = None
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -135,6 +204,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+            self.nvml.close()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -143,26 +216,29 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        if self.proc is None or not self.path:
+        if self.rows is not None:
+            rows, source = self.rows, "nvml"
+        elif self.proc is None or not self.path:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
-            except ValueError:
-                continue
-        os.unlink(self.path)
+        else:
+            rows, source = [], "nvidia-smi"
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+            os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, _, flags in rows for i, f in enumerate(flags) if f.lower() == "active"})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": source}
+        reasons = sorted({REASON_NAMES[i] for _, _, _, flags in rows for i, f in enumerate(flags) if f.lower() == "active"})
         pmax = max(r[2] for r in rows)
         loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
         return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded), "power_w_max": pmax}
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded), "power_w_max": pmax,
+                "source": source}
 
 
 def recorded_traffic(kernel_key: str):
@@ -580,7 +656,8 @@ def run_ours(args, parts_names):
                                          "measured_sustained": peaks.get("bf16_tflops_sustained")}},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"],
-                   "samples": clk["samples"], "samples_under_load": clk.get("samples_under_load")},
+                   "samples": clk["samples"], "samples_under_load": clk.get("samples_under_load"),
+                   "source": clk.get("source")},
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -65,6 +65,22 @@ def test_clock_sampler_parses_samples(tmp_path):
     assert s["reasons"] == ["sw_power_cap"]
 
 
+def test_clock_sampler_nvml_samples():
+    # NVML's reason bits: 0x4 software power cap, 0x8 hardware slowdown, 0x20 software
+    # thermal, 0x40 hardware thermal (the NVML header's nvmlClocksEventReason* values).
+    assert bench.nvml_reason_flags(0x0) == ["Not Active"] * 4
+    assert bench.nvml_reason_flags(0x48) == ["Active", "Active", "Not Active", "Not Active"]
+    assert bench.nvml_reason_flags(0x24) == ["Not Active", "Not Active", "Active", "Active"]
+    cs = bench.ClockSampler(0)
+    cs.rows = [(1980.0, 2070.0, 1200.5, bench.nvml_reason_flags(0x4)),
+               (1965.0, 2070.0, 1350.0, bench.nvml_reason_flags(0x4)),
+               (2070.0, 2070.0, 150.0, bench.nvml_reason_flags(0x1))]      # idle sample
+    s = cs.summary()
+    assert s["source"] == "nvml" and s["samples"] == 3 and s["samples_under_load"] == 2
+    assert s["sm_mhz"] == pytest.approx(1972.5)
+    assert s["reasons"] == ["sw_power_cap"]
+
+
 def test_recorded_traffic_needs_current_sources():
     # Returns an int only for a workload listed with the current source digest, else None.
     v = bench.recorded_traffic("no_such_workload")
