@@ -341,10 +341,9 @@ struct TileCoord {
     bool nhalf;
 };
 
-// Device-counts MoE schedule, built in shared memory by every CTA at start:
-// tile_pref[g] = tiles of experts before g, row_off[g] = rows before g.
-// Shared-memory prefix tables (null when a launch has none).  MoE: tiles and rows before
-// each expert, [G + 1] each.  Grouped: tile_pref[i] = problem i's first tile.
+// Shared-memory prefix tables, built by every CTA at start (null when a launch has none).
+// Device-counts MoE: tile_pref[g] = tiles of experts before g, row_off[g] = rows before g,
+// [G + 1] each.  Grouped: tile_pref[i] = problem i's first tile.
 struct MoeTable {
     const int32_t* tile_pref;
     const int32_t* row_off;
